@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Attention-forward benchmark: TFLOP/s (bf16) and fraction of dense-BF16 peak.
+
+One step is one exact attention forward (QK^T, online softmax, PV, O and
+LSE) over the whole workload, i.e. one launch of the library's kernel.  The
+default workload is B=2, H=32, N=4096, d=128, causal.  FLOPs per step are
+4*B*H*Nq*Nk*d, halved for causal.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+With N > 1 (torchrun), every rank runs its own copy of the workload: the
+units are independent (batch, head, query block) problems, so there is no
+collective on the data path ("scaling": "weak"); the barrier and the
+max-over-ranks timing are the only cross-rank steps.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOP/s bf16 (N=4096,d=128,causal) and % of dense-BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["exact_attention_42_gb300/csrc/fa_fwd.cu", "exact_attention_42_gb300/csrc/ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+ROTATE = 3            # input copies cycled through, so each step reads from HBM
+L2_BYTES = 129 * 2 ** 20
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget-s", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- helpers
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            flat = {}
+
+            def walk(x, pre=""):
+                if isinstance(x, dict):
+                    for k, v in x.items():
+                        walk(v, k if not pre else pre + "." + k)
+                elif isinstance(x, (int, float)):
+                    flat[pre.split(".")[-1]] = float(x)
+            walk(d)
+            if "bf16_tflops" in flat:
+                return {"hbm_gbs": flat.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]),
+                        "bf16_tflops": flat["bf16_tflops"],
+                        "bf16_tflops_sustained": flat.get("bf16_tflops_sustained", flat["bf16_tflops"]),
+                        "source": "measured"}
+        except (OSError, ValueError):
+            pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def load_traffic(workload: str):
+    """ncu DRAM bytes per launch, if captured for this exact kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernel_sha") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.proc = None
+        self.path = None
+        self.gpu_id = gpu_id
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="fa_clocks_", suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "200"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        try:
+            sm = [float(r[1]) for r in rows]
+            smax = max(float(r[2]) for r in rows)
+        except ValueError:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons,
+                "samples": len(rows), "power_w_median": statistics.median(
+                    [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()] or [0.0])}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    """Maximum of `value` over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def workload_config(prob, name):
+    cfg = {"workload": name, "B": prob.B, "Hq": prob.Hq, "Hkv": prob.Hkv, "Nq": prob.Nq, "Nk": prob.Nk,
+           "d": prob.d, "causal": prob.causal, "flop_per_step": prob.flops()}
+    if prob.varlen:
+        cfg["seqlens"] = prob.seqlens()
+        cfg["total_tokens"] = int(prob.cu_seqlens[-1])
+    return cfg
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample(prob, budget_s: float, start_head: int = 0):
+    """Times the fp64 oracle, as it stands, on whole heads of the workload
+    until `budget_s` is spent (at least one head).  Returns (TFLOP/s, threads,
+    description)."""
+    import numpy as np
+    from fa_inputs import bf16_bits_to_f64
+    from oracle import attention_fwd, oracle_threads
+
+    flops = 0.0
+    heads = 0
+    t0 = time.perf_counter()
+    hq = start_head
+    while True:
+        if prob.varlen:
+            s = hq % prob.B
+            h = (hq // prob.B) % prob.Hq
+            t_0, t_1 = int(prob.cu_seqlens[s]), int(prob.cu_seqlens[s + 1])
+            L = t_1 - t_0
+            kvh = h // (prob.Hq // prob.Hkv)
+            q = bf16_bits_to_f64(prob.q[h:h + 1, t_0:t_1])[None]
+            k = bf16_bits_to_f64(prob.k[kvh:kvh + 1, t_0:t_1])[None]
+            v = bf16_bits_to_f64(prob.v[kvh:kvh + 1, t_0:t_1])[None]
+            f = 4.0 * L * L * prob.d * (0.5 if prob.causal else 1.0)
+        else:
+            b = (hq // prob.Hq) % prob.B
+            h = hq % prob.Hq
+            kvh = h // (prob.Hq // prob.Hkv)
+            q = bf16_bits_to_f64(prob.q[b:b + 1, h:h + 1])
+            k = bf16_bits_to_f64(prob.k[b:b + 1, kvh:kvh + 1])
+            v = bf16_bits_to_f64(prob.v[b:b + 1, kvh:kvh + 1])
+            f = 4.0 * prob.Nq * prob.Nk * prob.d * (0.5 if prob.causal else 1.0)
+        attention_fwd(q, k, v, prob.scale, prob.causal)
+        flops += f
+        heads += 1
+        hq += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    desc = "%d whole head(s) of %s (every query row of each), fp64, %.1f s" % (heads, prob.name, dt)
+    return flops / dt / 1e12, oracle_threads(), desc, dt
+
+
+def run_reference(args):
+    """The oracle on the host cores, on the same workload and metric."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    from fa_inputs import make_workload, HEADLINE
+    name = args.workload or HEADLINE
+    prob = make_workload(name)
+    per_step = max(1.0, args.cpu_budget_s / max(1, args.steps))
+    for w in range(args.warmup):
+        oracle_sample(prob, 0.0, start_head=w)
+    vals, secs, descs = [], [], []
+    t0 = time.perf_counter()
+    threads = None
+    for i in range(args.steps):
+        v, threads, desc, dt = oracle_sample(prob, per_step, start_head=i * 7)
+        vals.append(v)
+        secs.append(dt)
+        descs.append(desc)
+    wall = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": workload_config(prob, name),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "per step: " + descs[-1]},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU run
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_setup()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import exact_attention_42_gb300 as fa
+    if rank == 0:
+        fa.build()
+    barrier(world, dev)
+    fa.lib()
+
+    from fa_inputs import make_workload, HEADLINE
+    name = args.workload or HEADLINE
+    prob = make_workload(name)
+    flops = prob.flops()
+
+    def dev_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q0, k0, v0 = dev_bf16(prob.q), dev_bf16(prob.k), dev_bf16(prob.v)
+    cu = None if prob.cu_seqlens is None else torch.from_numpy(prob.cu_seqlens).to(dev)
+    sets = []
+    for r in range(ROTATE):
+        q, k, v = (q0, k0, v0) if r == 0 else (q0.clone(), k0.clone(), v0.clone())
+        o = torch.empty_like(q)
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
+        sets.append((q, k, v, o, lse))
+    step_bytes = sum(t.numel() * t.element_size() for t in sets[0])
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        q, k, v, o, lse = sets[i % ROTATE]
+        fa.fwd(q, k, v, causal=prob.causal, scale=prob.scale, cu_seqlens=cu, out=o, lse=lse, stream=stream)
+
+    fa.fa_device_status()
+    sampler = None
+    if not args.no_clocks:
+        gid = None
+        try:
+            gid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+        except Exception:
+            gid = None
+        sampler = ClockSampler(gid)
+        sampler.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    clocks = sampler.stop() if sampler else None
+    ms_total = ev0.elapsed_time(ev1)
+    ms_step = reduce_max(ms_total / args.steps, world, dev)
+    status_bits = fa.fa_device_status()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # End to end through the public API: pinned host inputs copied in, the
+    # kernel, O and LSE copied back, every step.
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q0, k0, v0))
+    oh = torch.empty(q0.shape, dtype=torch.bfloat16, pin_memory=True)
+    lh = torch.empty(q0.shape[:-1], dtype=torch.float32, pin_memory=True)
+    q, k, v, o, lse = sets[0]
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * 2 + lh.numel() * 4
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        fa.fwd(q, k, v, causal=prob.causal, scale=prob.scale, cu_seqlens=cu, out=o, lse=lse, stream=stream)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / args.e2e_steps, world, dev)
+    e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
+
+    peaks = load_peaks()
+    achieved = flops / (ms_total / args.steps * 1e-3) / 1e12
+    tag = "of measured" if peaks["source"] == "measured" else "of fallback"
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": load_traffic(name),
+                "peak_kind": "bf16 dense burst " + tag,
+                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                "kernel": "fa_fwd_kernel", "algorithmic_flop_per_launch": flops,
+                "algorithmic_bytes_per_launch": prob.io_bytes()}
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": dict(workload_config(prob, name), parallelism="replicas" if world > 1 else "single",
+                           l2="inputs rotated over %d copies (%.0f MB > %d MB L2)"
+                              % (ROTATE, ROTATE * step_bytes / 1e6, L2_BYTES // 2 ** 20)),
+            "roofline": roofline,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "device_status": status_bits,
+            "kernel_sha": kernel_hash()}
+    if rank == 0 and not args.no_cpu_baseline:
+        v_cpu, threads, desc, _ = oracle_sample(prob, args.cpu_budget_s)
+        line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0 if status_bits == 0 else 1
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

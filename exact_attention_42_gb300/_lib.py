@@ -1,0 +1,79 @@
+"""ctypes binding of libfa.so: the C-ABI entry points, same names, no logic."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH
+
+FA_OK = 0
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_SHAPE", 3: "FA_ERR_ALIGN", 4: "FA_ERR_UNSUPPORTED",
+                5: "FA_ERR_CUDA", 6: "FA_ERR_TIMEOUT", 7: "FA_ERR_VALUE"}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class FaError(RuntimeError):
+    """A non-zero fa_status returned by the library."""
+
+    def __init__(self, status: int, what: str = "fa_fwd"):
+        self.status = status
+        super().__init__("%s failed: %s" % (what, fa_status_string(status)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libfa.so is not built (%s); run exact_attention_42_gb300.build.build()"
+                                   % LIB_PATH)
+            L = ctypes.CDLL(LIB_PATH)
+            vp, ci = ctypes.c_void_p, ctypes.c_int
+            L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, ci, vp, vp]
+            L.fa_fwd.restype = ci
+            L.fa_status_string.argtypes = [ci]
+            L.fa_status_string.restype = ctypes.c_char_p
+            L.fa_device_status.argtypes = [ctypes.POINTER(ci)]
+            L.fa_device_status.restype = ci
+            L.fa_fwd_smem_bytes.argtypes = [ci]
+            L.fa_fwd_smem_bytes.restype = ci
+            L.fa_fwd_threads.argtypes = []
+            L.fa_fwd_threads.restype = ci
+            _lib = L
+    return _lib
+
+
+def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens, stream) -> int:
+    """Direct call of the C entry point with integer addresses; returns the status."""
+    return lib().fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, ctypes.c_float(scale), int(causal),
+                        cu_seqlens, stream)
+
+
+def fa_status_string(status: int) -> str:
+    try:
+        return lib().fa_status_string(int(status)).decode()
+    except RuntimeError:
+        return STATUS_NAMES.get(int(status), "unknown status %d" % status)
+
+
+def fa_device_status() -> int:
+    """Reads and clears the device status word (synchronises the device)."""
+    bits = ctypes.c_int(0)
+    st = lib().fa_device_status(ctypes.byref(bits))
+    if st not in (0, 6):
+        raise FaError(st, "fa_device_status")
+    return bits.value
+
+
+def fa_fwd_smem_bytes(d: int) -> int:
+    return lib().fa_fwd_smem_bytes(d)
+
+
+def fa_fwd_threads() -> int:
+    return lib().fa_fwd_threads()

@@ -1,0 +1,103 @@
+"""PyTorch-facing wrapper: checks tensors, allocates outputs, calls fa_fwd.
+
+PyTorch supplies device memory and the current stream only; every step of
+the attention computation runs in the library's CUDA kernel.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from ._lib import FaError, fa_fwd
+
+
+def _check(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int, device) -> None:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.dim() != ndim:
+        raise ValueError("%s must have %d dims, got shape %s" % (name, ndim, tuple(t.shape)))
+    if not t.is_cuda or (device is not None and t.device != device):
+        raise ValueError("%s must be on the same CUDA device as q" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+        scale: Optional[float] = None, cu_seqlens: Optional[torch.Tensor] = None,
+        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+        stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Exact attention forward on the GPU; returns (O, LSE).
+
+    Dense: q [B, Hq, Nq, d], k/v [B, Hkv, Nk, d] -> O like q, LSE [B, Hq, Nq] fp32.
+    Packed (cu_seqlens int32 [nseq+1] on the device): q [Hq, T, d], k/v [Hkv, T, d]
+    -> O [Hq, T, d], LSE [Hq, T].  Inputs are bf16, contiguous, on one GPU; d is
+    64 or 128; scale defaults to 1/sqrt(d).  Runs on ``stream`` (default: the
+    current stream) without synchronising.
+    """
+    dev = q.device
+    packed = cu_seqlens is not None
+    nd = 3 if packed else 4
+    _check(q, "q", torch.bfloat16, nd, None)
+    _check(k, "k", torch.bfloat16, nd, dev)
+    _check(v, "v", torch.bfloat16, nd, dev)
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    if packed:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, 1, dev)
+        Hq, T, d = q.shape
+        Hkv, Tk, dk = k.shape
+        if Tk != T or dk != d:
+            raise ValueError("packed q, k, v must share the token count and head dim")
+        B, Nq, Nk = cu_seqlens.numel() - 1, T, T
+        o_shape, lse_shape = (Hq, T, d), (Hq, T)
+    else:
+        B, Hq, Nq, d = q.shape
+        Bk, Hkv, Nk, dk = k.shape
+        if Bk != B or dk != d:
+            raise ValueError("q and k must share batch size and head dim")
+        o_shape, lse_shape = (B, Hq, Nq, d), (B, Hq, Nq)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(o_shape, dtype=torch.bfloat16, device=dev)
+    else:
+        _check(out, "out", torch.bfloat16, nd, dev)
+        if tuple(out.shape) != o_shape:
+            raise ValueError("out has shape %s, expected %s" % (tuple(out.shape), o_shape))
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=dev)
+    else:
+        _check(lse, "lse", torch.float32, nd - 1, dev)
+        if tuple(lse.shape) != lse_shape:
+            raise ValueError("lse has shape %s, expected %s" % (tuple(lse.shape), lse_shape))
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    B, Hq, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                    cu_seqlens.data_ptr() if packed else None, s.cuda_stream)
+    if st != 0:
+        raise FaError(st)
+    return out, lse
+
+
+def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+             scale: Optional[float] = None, cu_seqlens: Optional[torch.Tensor] = None,
+             device: Optional[torch.device] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The same call for host tensors: copies inputs to the GPU, runs ``fwd``,
+    copies O and LSE back to (pinned, when the inputs are pinned) host memory
+    and waits for the result."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    nb = q.is_pinned()
+    qd, kd, vd = (t.to(device, non_blocking=nb) for t in (q, k, v))
+    cud = None if cu_seqlens is None else cu_seqlens.to(device, non_blocking=nb)
+    o, lse = fwd(qd, kd, vd, causal=causal, scale=scale, cu_seqlens=cud)
+    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=nb)
+    lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=nb)
+    oh.copy_(o, non_blocking=nb)
+    lh.copy_(lse, non_blocking=nb)
+    torch.cuda.current_stream(device).synchronize()
+    return oh, lh

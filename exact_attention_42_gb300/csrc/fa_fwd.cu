@@ -1,0 +1,730 @@
+// Exact attention forward for GB300 (sm_103a): tcgen05 tensor cores with
+// S and O accumulators in Tensor Memory, TMA-fed K/V ring, warp-specialised
+// load / MMA / softmax roles, and an online softmax with conditional rescale.
+//
+// Method ("FlashAttention面试讲解" interview canvas): K/V are moved tile by
+// tile into on-chip memory and, for each tile, QK^T, the online softmax and
+// the PV accumulation are done together so the N x N matrix never reaches HBM
+// (element flash-text); the softmax keeps a running max m, a running sum l and
+// the output accumulator O, and rescales old O and l by exp(m_old - m_new)
+// when the max grows (elements formula-text, qa2-a).  The Blackwell notes of
+// the same canvas (element v4-card-body) motivate the layout: accumulators in
+// TMEM, a fully asynchronous MMA pipeline, and a conditional rescale.  The
+// producer/consumer split and the idea of hiding one tile's softmax behind
+// another tile's matrix products come from the Hopper pipeline canvas
+// ("FlashAttention v3 Hopper asynchrony", elements pseudo-code and
+// pipeline-note); here the two consumers are two 128-row Q tiles that share
+// every K/V tile.
+//
+// CTA layout (384 threads, one CTA per SM, persistent over work units):
+//   warps 0-3  softmax for Q tile 0 (thread r owns row r = TMEM lane r)
+//   warps 4-7  softmax for Q tile 1
+//   warp 8     TMA producer (one lane): Q tiles, then K_j, V_j into the ring
+//   warp 9     MMA issuer (one lane) and TMEM owner
+//   warps 10-11 idle (they complete the third warpgroup for the register split)
+// TMEM (512 columns x 128 lanes, fp32):
+//   [0,128)   S_0   (P_0 as packed bf16 pairs overwrites columns [0,64))
+//   [128,256) S_1   (P_1 likewise)
+//   [256,384) O_0   [384,512) O_1   (d = 64 uses the first 64 of each)
+// A work unit is 256 consecutive query rows (two tiles) of one head.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <cstring>
+#include <cmath>
+#include <mutex>
+
+#include "fa.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr int BLOCK_M = 128;      // query rows per tile (= TMEM lanes)
+constexpr int BLOCK_N = 128;      // keys per K/V tile
+constexpr int NQT = 2;            // query tiles per CTA
+constexpr int UNIT_ROWS = BLOCK_M * NQT;
+constexpr int NUM_THREADS = 384;  // three warpgroups
+constexpr int WARP_PRODUCER = 8;
+constexpr int WARP_MMA = 9;
+// Register split.  The kernel is launched at 168 registers per thread (the
+// most 12 warps allow: three warps share each sub-partition's 16K registers).
+// The two softmax warpgroups then grow to REG_SOFTMAX and the load/MMA
+// warpgroup shrinks to REG_OTHER: 8*216 + 4*72 = 2016 = 12*168 (the block's
+// pool) and 2*216 + 72 = 504 <= 512 per sub-partition.
+constexpr int REG_LAUNCH = 168;
+constexpr int REG_SOFTMAX = 216;
+constexpr int REG_OTHER = 72;
+static_assert(8 * REG_SOFTMAX + 4 * REG_OTHER <= 12 * REG_LAUNCH, "register split exceeds the launch pool");
+static_assert(2 * REG_SOFTMAX + REG_OTHER <= 512, "register split exceeds a sub-partition");
+// Conditional rescale threshold in log2 units: the running max used for the
+// exponentials is only moved when a new row max exceeds it by more than TAU,
+// so unnormalised probabilities stay below 2^TAU.  O / l is unchanged by the
+// choice because P and l always share the same stale max.
+constexpr float TAU = 8.0f;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+
+// Device status word: bit (1 << role) is set when that role gave up waiting.
+__device__ int g_fa_status;
+
+template <int D>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int TILE_BYTES = BLOCK_M * D * 2;   // one 128 x D bf16 tile
+  static constexpr int CHUNKS = D / 64;                // 128-byte swizzle column blocks
+  static constexpr int CHUNK_BYTES = BLOCK_M * 128;    // 16 KB
+  static constexpr int NS = (D == 128) ? 5 : 8;        // K/V ring slots
+  static constexpr int SMEM_Q = NQT * TILE_BYTES;
+  static constexpr int SMEM_RING = NS * TILE_BYTES;
+  // barriers: full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int NUM_BARS = 2 * NS + 5 * NQT + 1;
+  static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + NUM_BARS * 8 + 16;
+};
+
+struct Params {
+  __nv_bfloat16* o;
+  float* lse;
+  const int* cu_seqlens;  // null: dense
+  int B, Hq, Hkv, Nq, Nk, group;
+  float scale_log2;       // scale * log2(e)
+  int causal;
+  int nqb;                // dense: query units per head = ceil(Nq / 256)
+  int num_units;          // dense: B * Hq * nqb; packed: computed on the device
+};
+
+struct Unit {
+  int Lq, Lk;        // sequence lengths (queries, keys)
+  int row0;          // first query row of the unit, local to the sequence
+  int q_y, k_y;      // TMA row coordinate of the sequence's first token
+  int q_z, k_z;      // TMA head coordinate
+  long long out_row; // global row index (in O / LSE rows) of the sequence's token 0
+};
+
+__device__ __forceinline__ int clampi(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
+
+// Unit u -> (sequence, head, query block).  Dense units are ordered
+// longest-first under a causal mask: the last query blocks of every head come
+// first, so the persistent CTAs start on the heaviest work.
+__device__ __forceinline__ bool decode_unit(const Params& p, int u, Unit& w) {
+  if (p.cu_seqlens == nullptr) {
+    const int bh_count = p.B * p.Hq;
+    const int qb = p.nqb - 1 - u / bh_count;
+    const int bh = u % bh_count;
+    const int b = bh / p.Hq, h = bh % p.Hq;
+    w.Lq = p.Nq;
+    w.Lk = p.Nk;
+    w.row0 = qb * UNIT_ROWS;
+    w.q_y = 0;
+    w.k_y = 0;
+    w.q_z = bh;
+    w.k_z = b * p.Hkv + h / p.group;
+    w.out_row = static_cast<long long>(bh) * p.Nq;
+    return true;
+  }
+  // Packed sequences: u = blk * Hq + h, blk enumerates every sequence's query
+  // blocks in order, the last block of a sequence first.
+  const int h = u % p.Hq;
+  int blk = u / p.Hq;
+  const int T = p.Nq;
+  int prev = clampi(__ldg(p.cu_seqlens), 0, T);
+  for (int s = 0; s < p.B; ++s) {
+    const int next = clampi(__ldg(p.cu_seqlens + s + 1), prev, T);
+    const int L = next - prev;
+    const int nb = (L + UNIT_ROWS - 1) / UNIT_ROWS;
+    if (blk < nb) {
+      w.Lq = L;
+      w.Lk = L;
+      w.row0 = (nb - 1 - blk) * UNIT_ROWS;
+      w.q_y = prev;
+      w.k_y = prev;
+      w.q_z = h;
+      w.k_z = h / p.group;
+      w.out_row = static_cast<long long>(h) * T + prev;
+      return true;
+    }
+    blk -= nb;
+    prev = next;
+  }
+  return false;
+}
+
+__device__ __forceinline__ int packed_num_units(const Params& p) {
+  const int T = p.Nq;
+  int prev = clampi(__ldg(p.cu_seqlens), 0, T);
+  int total = 0;
+  for (int s = 0; s < p.B; ++s) {
+    const int next = clampi(__ldg(p.cu_seqlens + s + 1), prev, T);
+    total += (next - prev + UNIT_ROWS - 1) / UNIT_ROWS;
+    prev = next;
+  }
+  return total * p.Hq;
+}
+
+// Number of K/V tiles query tile t of unit w must visit (0: no key visible).
+__device__ __forceinline__ int kv_tiles(const Params& p, const Unit& w, int t) {
+  const int q0 = w.row0 + t * BLOCK_M;
+  if (q0 >= w.Lq || w.Lk <= 0) return 0;
+  int last_key = w.Lk - 1;
+  if (p.causal) {
+    const int last_row = min(q0 + BLOCK_M - 1, w.Lq - 1);
+    last_key = min(last_key, last_row + (w.Lk - w.Lq));
+    if (last_key < 0) return 0;
+  }
+  return last_key / BLOCK_N + 1;
+}
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag, int role) {
+  *abort_flag = 1;
+  atomicOr(&g_fa_status, 1 << role);
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              int role) {
+  if (mbar_wait(bar, parity, abort_flag, WAIT_LIMIT_NS)) return true;
+  if (!*abort_flag) raise_abort(abort_flag, role);
+  return false;
+}
+
+// Teardown waits ignore the abort flag: they only wait for copies and MMAs
+// that were already issued, which complete on their own.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, volatile int* abort_flag, int role) {
+  __shared__ int never;
+  never = 0;
+  if (!mbar_wait(bar, parity, &never, WAIT_LIMIT_NS)) raise_abort(abort_flag, role);
+}
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + C::SMEM_Q;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + C::SMEM_RING);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const uint32_t bar_base = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (C::NS + s); };
+  auto qfull_bar = [&](int t) { return bar_base + 8u * (2 * C::NS + t); };
+  auto qempty_bar = [&](int t) { return bar_base + 8u * (2 * C::NS + NQT + t); };
+  auto sfull_bar = [&](int t) { return bar_base + 8u * (2 * C::NS + 2 * NQT + t); };
+  auto pfull_bar = [&](int t) { return bar_base + 8u * (2 * C::NS + 3 * NQT + t); };
+  auto odone_bar = [&](int t) { return bar_base + 8u * (2 * C::NS + 4 * NQT + t); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * C::NS + 5 * NQT);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int t = 0; t < NQT; ++t) {
+      mbar_init(qfull_bar(t), 1);
+      mbar_init(qempty_bar(t), 1);
+      mbar_init(sfull_bar(t), 1);
+      mbar_init(pfull_bar(t), BLOCK_M);
+      mbar_init(odone_bar(t), 1);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_num_units(p);
+
+  if (warp >= 8) {
+  setmaxnreg_dec<REG_OTHER>();
+  if (warp == WARP_PRODUCER) {
+    // ------------------------------------------------------------------ TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      if (p.Nk > 0) {  // with no keys the K/V maps are left unencoded and never used
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+      }
+      uint32_t it = 0;
+      uint32_t qfills[NQT] = {0, 0};
+      bool ok = true;
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        Unit w;
+        if (!decode_unit(p, u, w)) continue;
+        int nkv[NQT];
+        int nmax = 0;
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          nkv[t] = kv_tiles(p, w, t);
+          nmax = max(nmax, nkv[t]);
+        }
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (!ok || nkv[t] == 0) continue;
+          if (!(ok = wait_or_abort(qempty_bar(t), (qfills[t] & 1u) ^ 1u, abort_flag, 0))) continue;
+          mbar_arrive_expect_tx(qfull_bar(t), C::TILE_BYTES);
+          const uint32_t dst = smem_u32(sQ + t * C::TILE_BYTES);
+          for (int c = 0; c < C::CHUNKS; ++c)
+            tma_load_3d(dst + c * C::CHUNK_BYTES, &tm_q, qfull_bar(t), c * 64, w.q_y + w.row0 + t * BLOCK_M,
+                        w.q_z);
+          ++qfills[t];
+        }
+        for (int j = 0; j < nmax && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int s = it % C::NS;
+            if (!(ok = wait_or_abort(empty_bar(s), ((it / C::NS) & 1u) ^ 1u, abort_flag, 0))) break;
+            mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
+            const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, full_bar(s), c * 64, w.k_y + j * BLOCK_N,
+                          w.k_z);
+            ++it;
+          }
+        }
+      }
+      // Wait until every issued copy has landed before the CTA may exit.
+      for (int s = 0; s < C::NS; ++s) {
+        if (it > static_cast<uint32_t>(s)) {
+          const uint32_t f = s + C::NS * ((it - 1 - s) / C::NS);
+          wait_drain(full_bar(s), (f / C::NS) & 1u, abort_flag, 0);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < NQT; ++t)
+        if (qfills[t] > 0) wait_drain(qfull_bar(t), (qfills[t] - 1) & 1u, abort_flag, 0);
+    }
+  } else if (warp == WARP_MMA) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(BLOCK_M, BLOCK_N, 0, 0);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(BLOCK_M, D, 0, 1);
+      const uint32_t sq_addr = smem_u32(sQ);
+      const uint32_t ring_addr = smem_u32(sRing);
+      // S_t = Q_t K^T: both operands K-major (head dim contiguous), 16 columns per MMA.
+      auto issue_qk = [&](int t, int slot) {
+        const uint32_t qa = sq_addr + t * C::TILE_BYTES;
+        const uint32_t kb = ring_addr + slot * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32;
+          umma_ss(tmem + t * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                  IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t (+)= P_t V: P from TMEM (bf16 pairs), V MN-major (head dim contiguous), 16 keys per MMA.
+      auto issue_pv = [&](int t, int slot, bool accumulate) {
+        const uint32_t vb = ring_addr + slot * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
+          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                  smem_desc_sw128(vb + kk * 16 * 128, C::CHUNK_BYTES, 1024), IDESC_PV,
+                  (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+      uint32_t it = 0;
+      uint32_t qcnt[NQT] = {0, 0}, pcnt[NQT] = {0, 0};
+      bool ok = true;
+      for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+        Unit w;
+        if (!decode_unit(p, u, w)) continue;
+        int nkv[NQT];
+        int nmax = 0;
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          nkv[t] = kv_tiles(p, w, t);
+          nmax = max(nmax, nkv[t]);
+        }
+        if (nmax == 0) continue;
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (!ok || nkv[t] == 0) continue;
+          ok = wait_or_abort(qfull_bar(t), qcnt[t] & 1u, abort_flag, 1);
+          ++qcnt[t];
+        }
+        if (!ok) break;
+        // K_0 for every active tile.
+        {
+          const int s = it % C::NS;
+          if (!(ok = wait_or_abort(full_bar(s), (it / C::NS) & 1u, abort_flag, 1))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < NQT; ++t) {
+            if (nkv[t] == 0) continue;
+            issue_qk(t, s);
+            umma_commit(sfull_bar(t));
+            if (nkv[t] == 1) umma_commit(qempty_bar(t));
+          }
+          umma_commit(empty_bar(s));
+          ++it;
+        }
+        for (int j = 0; j < nmax && ok; ++j) {
+          const int sv = it % C::NS;
+          if (!(ok = wait_or_abort(full_bar(sv), (it / C::NS) & 1u, abort_flag, 1))) break;
+          tc_fence_after();
+          ++it;
+          const bool has_next = j + 1 < nmax;
+          const int sk = it % C::NS;
+          bool k_ready = false;
+#pragma unroll
+          for (int t = 0; t < NQT; ++t) {
+            if (!ok || j >= nkv[t]) continue;
+            if (!(ok = wait_or_abort(pfull_bar(t), pcnt[t] & 1u, abort_flag, 1))) continue;
+            ++pcnt[t];
+            tc_fence_after();
+            issue_pv(t, sv, j > 0);
+            umma_commit(odone_bar(t));
+            if (j + 1 < nkv[t]) {
+              if (!k_ready) {
+                if (!(ok = wait_or_abort(full_bar(sk), (it / C::NS) & 1u, abort_flag, 1))) continue;
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_qk(t, sk);
+              umma_commit(sfull_bar(t));
+              if (j + 2 == nkv[t]) umma_commit(qempty_bar(t));
+            }
+          }
+          if (!ok) break;
+          umma_commit(empty_bar(sv));
+          if (has_next) {
+            umma_commit(empty_bar(sk));
+            ++it;
+          }
+        }
+      }
+      // Every MMA issued so far completes before the CTA may release TMEM.
+      umma_commit(drain_bar);
+      wait_drain(drain_bar, 0, abort_flag, 1);
+    }
+  }
+  } else {
+    setmaxnreg_inc<REG_SOFTMAX>();
+    // -------------------------------------------------------------- softmax
+    const int t = warp / 4;
+    const int r = threadIdx.x % 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 128;
+    const uint32_t tO = tmem + lane_base + 256 + t * 128;
+    const float sl2 = p.scale_log2;
+    const float NEG_INF = -INFINITY;
+    uint32_t scnt = 0, pvcnt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
+      Unit w;
+      if (!decode_unit(p, u, w)) continue;
+      const int q0 = w.row0 + t * BLOCK_M;
+      if (q0 >= w.Lq) continue;
+      const int nkv = kv_tiles(p, w, t);
+      const int row = q0 + r;
+      const bool row_ok = row < w.Lq;
+      const int diag = row + (w.Lk - w.Lq);  // last visible key under the causal mask
+      const int tile_diag = q0 + (w.Lk - w.Lq);
+      float m_used = NEG_INF;
+      float l = 0.f;
+      for (int j = 0; j < nkv; ++j) {
+        if (!(ok = wait_or_abort(sfull_bar(t), scnt & 1u, abort_flag, 2 + t))) break;
+        ++scnt;
+        tc_fence_after();
+        float s[BLOCK_N];
+#pragma unroll
+        for (int c0 = 0; c0 < BLOCK_N; c0 += 32) {
+          uint32_t raw[32];
+          tmem_ld32_wait(tS + c0, raw);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c0 + i] = __uint_as_float(raw[i]);
+        }
+        const int k0 = j * BLOCK_N;
+        const bool need_mask = (k0 + BLOCK_N > w.Lk) || (p.causal && k0 + BLOCK_N - 1 > tile_diag);
+        if (need_mask) {
+          const int lim = p.causal ? min(w.Lk - 1, diag) : (w.Lk - 1);
+#pragma unroll
+          for (int c = 0; c < BLOCK_N; ++c)
+            if (k0 + c > lim) s[c] = NEG_INF;
+        }
+        float mx = s[0];
+#pragma unroll
+        for (int c = 1; c < BLOCK_N; ++c) mx = fmaxf(mx, s[c]);
+        const float m_tile = mx * sl2;
+        const float m_new = fmaxf(m_used, m_tile);
+        const bool need = m_new > m_used + TAU;
+        if (j == 0) {
+          m_used = m_new;
+        } else if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
+          if (!(ok = wait_or_abort(odone_bar(t), (pvcnt - 1) & 1u, abort_flag, 2 + t))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t raw[32];
+            tmem_ld32_wait(tO + c0, raw);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) raw[i] = __float_as_uint(__uint_as_float(raw[i]) * alpha);
+            tmem_st32(tO + c0, raw);
+          }
+          l *= alpha;
+          if (need) m_used = m_new;
+        }
+        const float neg_base = (m_used == NEG_INF) ? 0.f : -m_used;
+        float rowsum = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < BLOCK_N; c0 += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = ex2_approx(fmaf(s[c0 + 2 * i], sl2, neg_base));
+            const float b = ex2_approx(fmaf(s[c0 + 2 * i + 1], sl2, neg_base));
+            rowsum += a + b;
+            pk[i] = pack_bf16x2(a, b);
+          }
+          tmem_st16(tS + c0 / 2, pk);
+        }
+        l += rowsum;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(pfull_bar(t));
+        ++pvcnt;
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ epilogue
+      if (nkv > 0) {
+        if (!(ok = wait_or_abort(odone_bar(t), (pvcnt - 1) & 1u, abort_flag, 2 + t))) break;
+        tc_fence_after();
+      }
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = p.o + (w.out_row + row) * D;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t raw[32];
+        if (nkv > 0) {
+          tmem_ld32_wait(tO + c0, raw);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) raw[i] = 0u;
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * inv_l, __uint_as_float(raw[2 * i + 1]) * inv_l);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (row_ok) {
+        const float lse = (l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+        p.lse[w.out_row + row] = lse;
+      }
+    }
+  }
+
+  // -------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ============================================================================
+// Host side
+// ============================================================================
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qres;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qres) ==
+            cudaSuccess &&
+        qres == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// [heads, rows, d] bf16 tensor, loaded as 128-row x 64-column boxes with the
+// 128-byte swizzle that the UMMA K-major / MN-major descriptors expect.
+static bool encode_rows_map(CUtensorMap* map, const void* base, int d, long long rows, long long heads) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
+  cuuint32_t box[3] = {64, BLOCK_M, 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct DeviceInfo {
+  bool ok = false;
+  bool supported = false;
+  int sms = 0;
+  bool attr_set[2] = {false, false};
+};
+
+static constexpr int kMaxDevices = 64;
+static DeviceInfo g_dev[kMaxDevices];
+static std::mutex g_dev_mutex;
+
+static fa_status device_info(int dev, DeviceInfo** out) {
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ok) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    di.supported = (major == 10 && minor == 3);
+    di.sms = sms;
+    di.ok = true;
+  }
+  if (!di.supported) return FA_ERR_UNSUPPORTED;
+  *out = &di;
+  return FA_OK;
+}
+
+template <int D>
+static fa_status launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Nq, int Nk, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  DeviceInfo* di = nullptr;
+  fa_status st = device_info(dev, &di);
+  if (st != FA_OK) return st;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    const int idx = (D == 128) ? 1 : 0;
+    if (!di->attr_set[idx]) {
+      if (cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES) !=
+          cudaSuccess)
+        return FA_ERR_CUDA;
+      di->attr_set[idx] = true;
+    }
+  }
+  const bool packed = cu_seqlens != nullptr;
+  alignas(64) CUtensorMap tq, tk, tv;
+  std::memset(&tq, 0, sizeof(tq));
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  if (packed) {
+    if (!encode_rows_map(&tq, q, D, Nq, Hq)) return FA_ERR_CUDA;
+    if (Nk > 0 && (!encode_rows_map(&tk, k, D, Nk, Hkv) || !encode_rows_map(&tv, v, D, Nk, Hkv))) return FA_ERR_CUDA;
+  } else {
+    if (!encode_rows_map(&tq, q, D, Nq, static_cast<long long>(B) * Hq)) return FA_ERR_CUDA;
+    if (Nk > 0 && (!encode_rows_map(&tk, k, D, Nk, static_cast<long long>(B) * Hkv) ||
+                   !encode_rows_map(&tv, v, D, Nk, static_cast<long long>(B) * Hkv)))
+      return FA_ERR_CUDA;
+  }
+  Params prm;
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.cu_seqlens = cu_seqlens;
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Nq = Nq;
+  prm.Nk = Nk;
+  prm.group = Hq / Hkv;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.causal = causal ? 1 : 0;
+  long long grid;
+  if (packed) {
+    prm.nqb = 0;
+    prm.num_units = -1;
+    // Upper bound on units: every sequence adds at most one partial block.
+    const long long bound = static_cast<long long>(Hq) * ((Nq + UNIT_ROWS - 1) / UNIT_ROWS + B);
+    grid = bound < di->sms ? bound : di->sms;
+  } else {
+    prm.nqb = (Nq + UNIT_ROWS - 1) / UNIT_ROWS;
+    const long long units = static_cast<long long>(B) * Hq * prm.nqb;
+    if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
+    prm.num_units = static_cast<int>(units);
+    grid = units < di->sms ? units : di->sms;
+  }
+  if (grid <= 0) return FA_OK;
+  fa_fwd_kernel<D><<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
+}
+
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                 int Nk, int d, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
+  if (Hq % Hkv != 0) return FA_ERR_SHAPE;
+  if (cu_seqlens != nullptr && Nq != Nk) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_VALUE;
+  if (B == 0 || Hq == 0 || Nq == 0) return FA_OK;
+  if (q == nullptr || o == nullptr || lse == nullptr) return FA_ERR_NULL;
+  if (Nk > 0 && (k == nullptr || v == nullptr)) return FA_ERR_NULL;
+  auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+  if (mis16(q) || mis16(o) || (Nk > 0 && (mis16(k) || mis16(v)))) return FA_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
+  if (cu_seqlens != nullptr && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return FA_ERR_ALIGN;
+  // Row and element offsets are 64-bit; the tensor-map row count must fit 32 bits.
+  if (cu_seqlens == nullptr && static_cast<long long>(B) * Hq > 0x7fffffffLL) return FA_ERR_SHAPE;
+  if (d == 128) return fa::launch<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens, stream);
+  return fa::launch<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens, stream);
+}
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_NULL: return "FA_ERR_NULL: a required pointer is NULL";
+    case FA_ERR_SHAPE: return "FA_ERR_SHAPE: invalid sizes";
+    case FA_ERR_ALIGN: return "FA_ERR_ALIGN: misaligned pointer";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim or device not supported";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call failed";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait timed out";
+    case FA_ERR_VALUE: return "FA_ERR_VALUE: scale must be finite and positive";
+  }
+  return "unknown fa_status";
+}
+
+fa_status fa_device_status(int* bits) {
+  if (bits == nullptr) return FA_ERR_NULL;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, fa::g_fa_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  *bits = v;
+  return v ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+int fa_fwd_smem_bytes(int d) {
+  if (d == 64) return fa::Cfg<64>::SMEM_BYTES;
+  if (d == 128) return fa::Cfg<128>::SMEM_BYTES;
+  return 0;
+}
+
+int fa_fwd_threads(void) { return fa::NUM_THREADS; }
+
+}  // extern "C"

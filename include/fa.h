@@ -1,0 +1,100 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact-attention forward library, libfa.so.
+ *
+ * What it computes.  Standard attention, exactly: S = scale * Q K^T, P = softmax(S)
+ * row by row, O = P V ("FlashAttention面试讲解" interview canvas, element std-text).
+ * The tiled method of the same canvas (elements flash-text, formula-text, qa2-a)
+ * visits K/V one tile at a time with an online softmax -- a running row maximum m,
+ * a running sum l and a rescaled output accumulator -- so the N x N score matrix is
+ * never written to memory.  The forward pass also keeps one per-row statistic for a
+ * backward pass (elements v1-card-body and qa3-a): here that is the natural-log
+ * logsumexp of the scaled scores, LSE_i = ln sum_j exp(S_ij) over the valid keys.
+ *
+ * Conventions fixed by this library (the pages leave them open):
+ *   - causal masks are bottom-right aligned: key j is visible to query i iff
+ *     j <= i + (Nk - Nq); with Nq == Nk this is the usual lower triangle;
+ *   - a query row that sees no key gets O = 0 and LSE = -inf;
+ *   - grouped-query attention: query head h reads key/value head h / (Hq / Hkv);
+ *   - P is rounded to bf16 before the P*V product; all accumulation is fp32.
+ *
+ * Thread safety: every entry point is reentrant.  The library keeps only
+ * once-initialised per-device launch settings and one device status word.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULL = 1,        /* a required pointer is NULL */
+  FA_ERR_SHAPE = 2,       /* negative size, Hkv < 1, Hq % Hkv != 0, or Nq != Nk with cu_seqlens */
+  FA_ERR_ALIGN = 3,       /* q, k, v or o not 16-byte aligned, or lse not 4-byte aligned */
+  FA_ERR_UNSUPPORTED = 4, /* d not in {64, 128}, or the current device is not sm_103 */
+  FA_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed while enqueueing */
+  FA_ERR_TIMEOUT = 6,     /* a kernel gave up on a bounded wait (reported by fa_device_status) */
+  FA_ERR_VALUE = 7        /* scale is not a finite positive number */
+} fa_status;
+
+/*
+ * fa_fwd -- exact attention forward, O and LSE, on `stream`.
+ *
+ * Dense mode (cu_seqlens == NULL), row-major and contiguous:
+ *   q   [B, Hq,  Nq, d]  bf16, device      k, v [B, Hkv, Nk, d] bf16, device
+ *   o   [B, Hq,  Nq, d]  bf16, device      lse  [B, Hq, Nq]     fp32, device
+ * Packed variable-length mode (cu_seqlens != NULL): B sequences are concatenated
+ * along the token axis; sequence s owns tokens [cu_seqlens[s], cu_seqlens[s+1]):
+ *   q, o [Hq, Nq, d], k, v [Hkv, Nq, d], lse [Hq, Nq], with Nq == Nk == total tokens.
+ *   cu_seqlens is an int32 device array of B+1 non-decreasing offsets, cu_seqlens[0]
+ *   == 0 and cu_seqlens[B] == Nq.  Queries attend only to keys of their own sequence
+ *   (the causal mask is applied per sequence).  Offsets are clamped to [0, Nq] on the
+ *   device, so malformed offsets give wrong results but never out-of-range accesses.
+ *
+ * scale: the factor applied to Q K^T, finite and > 0 (usually 1/sqrt(d)).
+ * causal: 0 or 1.
+ * d: 64 or 128.
+ *
+ * Ownership: the caller owns every buffer; the library allocates no device
+ * memory.  The call is asynchronous: it validates arguments on the host,
+ * enqueues one kernel on `stream` and returns.  Inputs must stay valid and
+ * outputs untouched until the stream reaches that point.
+ *
+ * Empty problems (B, Hq or Nq equal to 0) return FA_OK and launch nothing.
+ * With Nk == 0 every row is written as O = 0, LSE = -inf (k and v may be NULL).
+ *
+ * Errors: FA_ERR_NULL / SHAPE / ALIGN / UNSUPPORTED / VALUE are detected before
+ * anything is enqueued and leave the outputs untouched.  FA_ERR_CUDA reports a
+ * failed launch.  Device-side time-outs are recorded in the status word read by
+ * fa_device_status().
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                 const int32_t* cu_seqlens, cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* fa_status_string(fa_status s);
+
+/*
+ * fa_device_status -- reads and clears the device status word of the current
+ * device.  Every wait inside the kernels is bounded; a wait that runs out sets
+ * a bit in this word and the kernel leaves cleanly.  Returns FA_OK and stores
+ * 0 in *bits when nothing went wrong, FA_ERR_TIMEOUT with the bits otherwise.
+ * This call synchronises the device (it reads device memory).
+ */
+fa_status fa_device_status(int* bits);
+
+/* Dynamic shared memory (bytes) and threads per CTA used for head dim d;
+ * 0 for an unsupported d.  For tooling and tests. */
+int fa_fwd_smem_bytes(int d);
+int fa_fwd_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

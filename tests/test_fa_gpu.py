@@ -1,0 +1,188 @@
+"""GPU parity: the tcgen05 kernel, called through the C ABI, against the fp64
+CPU oracle on the same seeded bf16 inputs.
+
+Tolerances: max |O - O_ref| <= 2e-2 and |LSE - LSE_ref| <= 1e-3 * max(1, |LSE_ref|)
+(bf16 inputs, fp32 accumulation).  Small and medium shapes are compared
+element by element; the full-size workloads are compared on sampled rows,
+which the oracle computes one by one, in the same launch configuration the
+bench uses.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from fa_inputs import make_dense, make_varlen, make_workload, f64_to_bf16_bits, WORKLOADS
+from fa_testutil import run_gpu, oracle_full, compare, compare_sampled, sample_rows, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_42_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return torch.device("cuda", 0)
+
+
+@pytest.fixture(autouse=True)
+def _status_clean(fa):
+    fa.fa_device_status()
+    yield
+    assert fa.fa_device_status() == 0, "a kernel wait timed out"
+
+
+# ---------------------------------------------------------------- workloads
+
+@pytest.mark.parametrize("name", ["tiny_b1_h2_n128_d64", "b4_h16_n1024_d64", "b4_h16_n1024_d64_causal"])
+def test_workload_full(fa, dev, name):
+    prob = make_workload(name)
+    o, lse = run_gpu(fa, prob, dev)
+    ref_o, ref_lse = oracle_full(prob)
+    compare(o, lse, ref_o, ref_lse, name)
+
+
+@pytest.mark.parametrize("name", ["b2_h32_n4096_d128_causal", "gqa_b1_hq32_hkv8_n16384_d128_causal",
+                                  "varlen16_h16_d128_causal"])
+def test_workload_full_size_sampled(fa, dev, name):
+    prob = make_workload(name)
+    o, lse = run_gpu(fa, prob, dev, keep_on_device=True)
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+    compare_sampled(o, lse, prob, sample_rows(prob, 160, seed=sum(map(ord, name))))
+
+
+# ------------------------------------------------------------- edge shapes
+
+EDGE = [
+    # (B, Hq, Hkv, Nq, Nk, d, causal)
+    (2, 3, 3, 200, 200, 128, True),     # ragged tail, several tiles
+    (2, 3, 3, 200, 200, 128, False),
+    (1, 2, 1, 77, 300, 64, True),       # Nq < Nk: bottom-right diagonal
+    (1, 2, 2, 300, 77, 64, True),       # Nq > Nk: first rows see no key
+    (1, 2, 2, 300, 77, 128, False),
+    (1, 1, 1, 5, 5, 64, True),          # shorter than one tile
+    (1, 1, 1, 1, 1, 128, False),
+    (1, 1, 1, 1, 700, 128, True),       # one query row against many keys
+    (1, 32, 1, 130, 130, 128, True),    # MQA: 32 query heads on one KV head
+    (2, 8, 2, 257, 257, 64, True),      # GQA g=4, tile + 1 row
+    (1, 4, 4, 512, 512, 128, True),     # exact multiple of the 256-row unit
+    (3, 5, 5, 384, 640, 64, False),
+]
+
+
+@pytest.mark.parametrize("shape", EDGE, ids=["-".join(map(str, s)) for s in EDGE])
+def test_edge_shapes(fa, dev, shape):
+    B, Hq, Hkv, Nq, Nk, d, causal = shape
+    prob = make_dense(B, Hq, Hkv, Nq, Nk, d, seed=sum(shape), causal=causal, name="edge")
+    o, lse = run_gpu(fa, prob, dev)
+    ref_o, ref_lse = oracle_full(prob)
+    compare(o, lse, ref_o, ref_lse, str(shape))
+
+
+VARLEN = [
+    ([1, 127, 128, 129, 0, 300, 256, 257], 4, 2, 64, True),
+    ([1, 127, 128, 129, 0, 300, 256, 257], 4, 2, 128, False),
+    ([513, 3, 1000], 2, 2, 128, True),
+    ([0, 0, 64], 1, 1, 64, True),
+]
+
+
+@pytest.mark.parametrize("case", VARLEN, ids=["v%d" % i for i in range(len(VARLEN))])
+def test_varlen(fa, dev, case):
+    lens, Hq, Hkv, d, causal = case
+    prob = make_varlen(lens, Hq, Hkv, d, seed=len(lens) + d, causal=causal)
+    o, lse = run_gpu(fa, prob, dev)
+    ref_o, ref_lse = oracle_full(prob)
+    compare(o, lse, ref_o, ref_lse, "varlen %s" % lens)
+
+
+def test_no_keys(fa, dev):
+    prob = make_dense(1, 2, 2, 100, 0, 64, seed=3, causal=False)
+    o, lse = run_gpu(fa, prob, dev)
+    assert np.all(o == 0.0) and np.all(np.isneginf(lse))
+
+
+def test_growing_scores_force_rescales(fa, dev):
+    """Scores that grow along the key axis move the running max by more than
+    the rescale threshold in every K/V tile (exercises the O correction)."""
+    N, d = 1024, 128
+    # s_j = scale * 0.25 * d * k_j grows by about 20 (log2 units) per 128-key tile.
+    q = np.full((1, 2, N, d), 0.25)
+    ramp = np.linspace(0.0, 40.0, N)[None, None, :, None]
+    k = np.broadcast_to(ramp, (1, 2, N, d)) + 0.01 * np.random.default_rng(0).standard_normal((1, 2, N, d))
+    v = np.random.default_rng(1).standard_normal((1, 2, N, d))
+    for causal in (False, True):
+        prob = make_dense(1, 2, 2, N, N, d, seed=0, causal=causal)
+        prob.q, prob.k, prob.v = (f64_to_bf16_bits(x) for x in (q, k, v))
+        prob.scale = 1.0 / math.sqrt(d)
+        o, lse = run_gpu(fa, prob, dev)
+        ref_o, ref_lse = oracle_full(prob)
+        compare(o, lse, ref_o, ref_lse, "growing scores causal=%s" % causal)
+
+
+def test_large_score_magnitudes(fa, dev):
+    """Scores spanning hundreds of units (exp would overflow without the max)."""
+    prob = make_dense(1, 2, 2, 300, 300, 64, seed=21, causal=True)
+    prob.scale = 4.0
+    o, lse = run_gpu(fa, prob, dev)
+    ref_o, ref_lse = oracle_full(prob)
+    assert np.max(np.abs(ref_lse)) > 50
+    compare(o, lse, ref_o, ref_lse, "large scores")
+
+
+# ------------------------------------------------------------- properties
+
+def test_deterministic_and_stream(fa, dev):
+    prob = make_dense(2, 4, 2, 600, 600, 128, seed=5, causal=True)
+    q, k, v = (to_dev(x, dev) for x in (prob.q, prob.k, prob.v))
+    o1, l1 = fa.fwd(q, k, v, causal=True)
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        o2, l2 = fa.fwd(q, k, v, causal=True)
+    s.synchronize()
+    torch.cuda.synchronize(dev)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_output_canaries(fa, dev):
+    """Writes stay inside O and LSE (guard regions around both are untouched)."""
+    lens = [1, 130, 0, 255, 257]
+    prob = make_varlen(lens, 3, 1, 128, seed=9, causal=True)
+    q, k, v = (to_dev(x, dev) for x in (prob.q, prob.k, prob.v))
+    cu = torch.from_numpy(prob.cu_seqlens).to(dev)
+    T, G = int(prob.cu_seqlens[-1]), 4096
+    obuf = torch.full((G + 3 * T * 128 + G,), 7.0, dtype=torch.bfloat16, device=dev)
+    lbuf = torch.full((G + 3 * T + G,), 7.0, dtype=torch.float32, device=dev)
+    o = obuf[G:G + 3 * T * 128].view(3, T, 128)
+    l = lbuf[G:G + 3 * T].view(3, T)
+    fa.fwd(q, k, v, causal=True, cu_seqlens=cu, out=o, lse=l)
+    torch.cuda.synchronize(dev)
+    assert torch.all(obuf[:G] == 7.0) and torch.all(obuf[G + 3 * T * 128:] == 7.0)
+    assert torch.all(lbuf[:G] == 7.0) and torch.all(lbuf[G + 3 * T:] == 7.0)
+    ref_o, ref_lse = oracle_full(prob)
+    compare(o.float().cpu().numpy().astype(np.float64), l.cpu().numpy().astype(np.float64), ref_o, ref_lse, "canary")
+
+
+def test_misaligned_pointer_is_rejected(fa, dev):
+    buf = torch.zeros(1 * 1 * 64 * 64 + 8, dtype=torch.bfloat16, device=dev)
+    q = buf[1:1 + 64 * 64].view(1, 1, 64, 64)
+    k = torch.zeros(1, 1, 64, 64, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(fa.FaError) as e:
+        fa.fwd(q, k, k)
+    assert e.value.status == 3
+
+
+def test_host_entry_matches_device_entry(fa, dev):
+    prob = make_dense(1, 4, 4, 256, 256, 64, seed=13, causal=True)
+    qh, kh, vh = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (prob.q, prob.k, prob.v))
+    o_h, l_h = fa.fwd_host(qh, kh, vh, causal=True)
+    o_d, l_d = fa.fwd(qh.to(dev), kh.to(dev), vh.to(dev), causal=True)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
