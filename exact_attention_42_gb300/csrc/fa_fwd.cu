@@ -20,8 +20,12 @@
 //   warps 0-3  softmax for Q tile 0 (thread r owns row r = TMEM lane r)
 //   warps 4-7  softmax for Q tile 1
 //   warp 8     TMA producer (one lane): Q tiles, then K_j, V_j into the ring
-//   warp 9     MMA issuer (one lane) and TMEM owner
-//   warps 10-11 idle (they complete the third warpgroup for the register split)
+//   warp 9     MMA issuer for Q tile 0 (one lane) and TMEM owner
+//   warp 10    MMA issuer for Q tile 1 (one lane)
+//   warp 11    idle (it completes the third warpgroup for the register split)
+// One thread issues tcgen05.mma at most about once per 126 cycles, while a
+// 128x128x16 product takes about 70-80 cycles on the tensor pipe, so each
+// query tile has its own issuing thread; both consume the same K/V ring.
 // TMEM (512 columns x 128 lanes, fp32):
 //   [0,128)   S_0   (P_0 as packed bf16 pairs overwrites columns [0,64))
 //   [128,256) S_1   (P_1 likewise)
@@ -47,7 +51,7 @@ constexpr int NQT = 2;            // query tiles per CTA
 constexpr int UNIT_ROWS = BLOCK_M * NQT;
 constexpr int NUM_THREADS = 384;  // three warpgroups
 constexpr int WARP_PRODUCER = 8;
-constexpr int WARP_MMA = 9;
+constexpr int WARP_MMA = 9;  // warps WARP_MMA + t issue the products of query tile t
 // Register split.  The kernel is launched at 168 registers per thread (the
 // most 12 warps allow: three warps share each sub-partition's 16K registers).
 // The two softmax warpgroups then grow to REG_SOFTMAX and the load/MMA
@@ -224,7 +228,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), NQT);  // released by both tiles' MMA issuers
     }
     for (int t = 0; t < NQT; ++t) {
       mbar_init(qfull_bar(t), 1);
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(pfull_bar(t), BLOCK_M);
       mbar_init(odone_bar(t), 1);
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar, NQT);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -316,104 +320,96 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int t = 0; t < NQT; ++t)
         if (qfills[t] > 0) wait_drain(qfull_bar(t), (qfills[t] - 1) & 1u, abort_flag, 0);
     }
-  } else if (warp == WARP_MMA) {
+  } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
     // ------------------------------------------------------------------ MMA
+    // Thread t issues every product of query tile t.  Per tile the order is
+    // QK(0), then for each j: PV(j), QK(j+1); S_t is therefore overwritten by
+    // QK(j+1) only after PV(j) has read the P that aliases it (the products
+    // of one thread complete in issue order).
     if (lane == 0) {
+      const int t = warp - WARP_MMA;
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(BLOCK_M, BLOCK_N, 0, 0);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(BLOCK_M, D, 0, 1);
-      const uint32_t sq_addr = smem_u32(sQ);
+      const uint32_t tS = tmem + t * 128;
+      const uint32_t tO = tmem + 256 + t * 128;
+      const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ) + t * C::TILE_BYTES, 16, 1024);
       const uint32_t ring_addr = smem_u32(sRing);
       // S_t = Q_t K^T: both operands K-major (head dim contiguous), 16 columns per MMA.
-      auto issue_qk = [&](int t, int slot) {
-        const uint32_t qa = sq_addr + t * C::TILE_BYTES;
-        const uint32_t kb = ring_addr + slot * C::TILE_BYTES;
+      auto issue_qk = [&](int slot) {
+        const uint64_t k_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32;
-          umma_ss(tmem + t * 128, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                  IDESC_QK, kk > 0 ? 1u : 0u);
+          const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
+          umma_ss(tS, q_desc + off, k_desc + off, IDESC_QK, kk > 0 ? 1u : 0u);
         }
       };
       // O_t (+)= P_t V: P from TMEM (bf16 pairs), V MN-major (head dim contiguous), 16 keys per MMA.
-      auto issue_pv = [&](int t, int slot, bool accumulate) {
-        const uint32_t vb = ring_addr + slot * C::TILE_BYTES;
+      auto issue_pv = [&](int slot, bool accumulate) {
+        const uint64_t v_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
 #pragma unroll
         for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
-          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                  smem_desc_sw128(vb + kk * 16 * 128, C::CHUNK_BYTES, 1024), IDESC_PV,
+          umma_ts(tO, tS + kk * 8, v_desc + static_cast<uint64_t>(kk * 16 * 128 >> 4), IDESC_PV,
                   (accumulate || kk > 0) ? 1u : 0u);
         }
       };
-      uint32_t it = 0;
-      uint32_t qcnt[NQT] = {0, 0}, pcnt[NQT] = {0, 0};
+      // A ring slot this tile does not read is still released, after it has
+      // been filled, so both issuers arrive once per fill in fill order.
+      auto release = [&](int slot, bool used) {
+        if (used) umma_commit(empty_bar(slot));
+        else mbar_arrive(empty_bar(slot));
+      };
+      uint32_t it = 0, qcnt = 0, pcnt = 0;
       bool ok = true;
       for (int k = 0; k * static_cast<int>(gridDim.x) < num_units && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= num_units) continue;
         Unit w;
         if (!decode_unit(p, u, w)) continue;
-        int nkv[NQT];
-        int nmax = 0;
-#pragma unroll
-        for (int t = 0; t < NQT; ++t) {
-          nkv[t] = kv_tiles(p, w, t);
-          nmax = max(nmax, nkv[t]);
-        }
+        const int nkv = kv_tiles(p, w, t);
+        const int nmax = max(kv_tiles(p, w, 0), kv_tiles(p, w, 1));
         if (nmax == 0) continue;
-#pragma unroll
-        for (int t = 0; t < NQT; ++t) {
-          if (!ok || nkv[t] == 0) continue;
-          ok = wait_or_abort(qfull_bar(t), qcnt[t] & 1u, abort_flag, 1);
-          ++qcnt[t];
+        if (nkv > 0) {
+          if (!(ok = wait_or_abort(qfull_bar(t), qcnt & 1u, abort_flag, 1))) break;
+          ++qcnt;
         }
-        if (!ok) break;
-        // K_0 for every active tile.
+        // K_0
         {
           const int s = it % C::NS;
           if (!(ok = wait_or_abort(full_bar(s), (it / C::NS) & 1u, abort_flag, 1))) break;
           tc_fence_after();
-#pragma unroll
-          for (int t = 0; t < NQT; ++t) {
-            if (nkv[t] == 0) continue;
-            issue_qk(t, s);
+          if (nkv > 0) {
+            issue_qk(s);
             umma_commit(sfull_bar(t));
-            if (nkv[t] == 1) umma_commit(qempty_bar(t));
+            if (nkv == 1) umma_commit(qempty_bar(t));
           }
-          umma_commit(empty_bar(s));
+          release(s, nkv > 0);
           ++it;
         }
-        for (int j = 0; j < nmax && ok; ++j) {
+        for (int j = 0; j < nmax; ++j) {
           const int sv = it % C::NS;
           if (!(ok = wait_or_abort(full_bar(sv), (it / C::NS) & 1u, abort_flag, 1))) break;
           tc_fence_after();
           ++it;
-          const bool has_next = j + 1 < nmax;
-          const int sk = it % C::NS;
-          bool k_ready = false;
-#pragma unroll
-          for (int t = 0; t < NQT; ++t) {
-            if (!ok || j >= nkv[t]) continue;
-            if (!(ok = wait_or_abort(pfull_bar(t), pcnt[t] & 1u, abort_flag, 1))) continue;
-            ++pcnt[t];
+          if (j < nkv) {
+            if (!(ok = wait_or_abort(pfull_bar(t), pcnt & 1u, abort_flag, 1))) break;
+            ++pcnt;
             tc_fence_after();
-            issue_pv(t, sv, j > 0);
-            if (j + 1 == nkv[t]) umma_commit(odone_bar(t));  // last PV of this tile in the unit
-            if (j + 1 < nkv[t]) {
-              if (!k_ready) {
-                if (!(ok = wait_or_abort(full_bar(sk), (it / C::NS) & 1u, abort_flag, 1))) continue;
-                tc_fence_after();
-                k_ready = true;
-              }
-              issue_qk(t, sk);
-              umma_commit(sfull_bar(t));
-              if (j + 2 == nkv[t]) umma_commit(qempty_bar(t));
-            }
+            issue_pv(sv, j > 0);
+            if (j + 1 == nkv) umma_commit(odone_bar(t));  // last PV of this tile in the unit
           }
-          if (!ok) break;
-          umma_commit(empty_bar(sv));
-          if (has_next) {
-            umma_commit(empty_bar(sk));
+          release(sv, j < nkv);
+          if (j + 1 < nmax) {
+            const int sk = it % C::NS;
+            if (!(ok = wait_or_abort(full_bar(sk), (it / C::NS) & 1u, abort_flag, 1))) break;
+            tc_fence_after();
             ++it;
+            const bool use_k = j + 1 < nkv;
+            if (use_k) {
+              issue_qk(sk);
+              umma_commit(sfull_bar(t));
+              if (j + 2 == nkv) umma_commit(qempty_bar(t));
+            }
+            release(sk, use_k);
           }
         }
       }
