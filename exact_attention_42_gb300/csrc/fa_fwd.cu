@@ -19,13 +19,18 @@
 // CTA layout (384 threads, one CTA per SM, persistent over work units):
 //   warps 0-3  softmax for Q tile 0 (thread r owns row r = TMEM lane r)
 //   warps 4-7  softmax for Q tile 1
-//   warp 8     TMA producer (one lane): Q tiles, then K_j, V_j into the ring
-//   warp 9     MMA issuer for Q tile 0 (one lane) and TMEM owner
-//   warp 10    MMA issuer for Q tile 1 (one lane)
-//   warp 11    idle (it completes the third warpgroup for the register split)
-// One thread issues tcgen05.mma at most about once per 126 cycles, while a
-// 128x128x16 product takes about 70-80 cycles on the tensor pipe, so each
-// query tile has its own issuing thread; both consume the same K/V ring.
+//   warp 8     K/V producer (one lane): K_j, V_j of every unit into the ring
+//   warp 9     MMA issuer and TMEM owner: the whole warp runs the issue loop
+//              and one elected lane issues, which keeps descriptors and loop
+//              state warp-uniform (about 95 cycles per tcgen05.mma, against
+//              about 130 when a lone lane runs the loop)
+//   warp 10    idle
+//   warp 11    Q loader (one lane): reloads Q tile t as soon as the last QK of
+//              tile t in the previous unit has completed, so the K/V stream
+//              never stalls at a unit boundary
+// Products are issued in the order QK_0(0), QK_1(0), then per K/V tile j:
+// PV_0(j), QK_0(j+1), PV_1(j), QK_1(j+1).  Tile 0's softmax therefore runs
+// while the tensor pipe works on tile 1's products and the other way round.
 // TMEM (512 columns x 128 lanes, fp32):
 //   [0,128)   S_0   (P_0 as packed bf16 pairs overwrites columns [0,64))
 //   [128,256) S_1   (P_1 likewise)
@@ -52,6 +57,7 @@ constexpr int UNIT_ROWS = BLOCK_M * NQT;
 constexpr int NUM_THREADS = 384;  // three warpgroups
 constexpr int WARP_PRODUCER = 8;
 constexpr int WARP_MMA = 9;  // warps WARP_MMA + t issue the products of query tile t
+constexpr int WARP_QLOAD = 11;
 // Register split.  The kernel is launched at 168 registers per thread (the
 // most 12 warps allow: three warps share each sub-partition's 16K registers).
 // The two softmax warpgroups then grow to REG_SOFTMAX and the load/MMA
@@ -228,7 +234,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NS; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), NQT);  // released by both tiles' MMA issuers
+      mbar_init(empty_bar(s), 1);
     }
     for (int t = 0; t < NQT; ++t) {
       mbar_init(qfull_bar(t), 1);
@@ -237,7 +243,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(pfull_bar(t), BLOCK_M);
       mbar_init(odone_bar(t), 1);
     }
-    mbar_init(drain_bar, NQT);
+    mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -271,31 +277,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tma_prefetch_desc(&tm_v);
       }
       uint32_t it = 0;
-      uint32_t qfills[NQT] = {0, 0};
       bool ok = true;
       for (int k = 0; k * static_cast<int>(gridDim.x) < num_units && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= num_units) continue;
         Unit w;
         if (!decode_unit(p, u, w)) continue;
-        int nkv[NQT];
-        int nmax = 0;
-#pragma unroll
-        for (int t = 0; t < NQT; ++t) {
-          nkv[t] = kv_tiles(p, w, t);
-          nmax = max(nmax, nkv[t]);
-        }
-#pragma unroll
-        for (int t = 0; t < NQT; ++t) {
-          if (!ok || nkv[t] == 0) continue;
-          if (!(ok = wait_or_abort(qempty_bar(t), (qfills[t] & 1u) ^ 1u, abort_flag, 0))) continue;
-          mbar_arrive_expect_tx(qfull_bar(t), C::TILE_BYTES);
-          const uint32_t dst = smem_u32(sQ + t * C::TILE_BYTES);
-          for (int c = 0; c < C::CHUNKS; ++c)
-            tma_load_3d(dst + c * C::CHUNK_BYTES, &tm_q, qfull_bar(t), c * 64, w.q_y + w.row0 + t * BLOCK_M,
-                        w.q_z);
-          ++qfills[t];
-        }
+        const int nmax = max(kv_tiles(p, w, 0), kv_tiles(p, w, 1));
         for (int j = 0; j < nmax && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv) {
             const int s = it % C::NS;
@@ -316,107 +304,145 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           wait_drain(full_bar(s), (f / C::NS) & 1u, abort_flag, 0);
         }
       }
-#pragma unroll
-      for (int t = 0; t < NQT; ++t)
-        if (qfills[t] > 0) wait_drain(qfull_bar(t), (qfills[t] - 1) & 1u, abort_flag, 0);
     }
-  } else if (warp == WARP_MMA || warp == WARP_MMA + 1) {
-    // ------------------------------------------------------------------ MMA
-    // Thread t issues every product of query tile t.  Per tile the order is
-    // QK(0), then for each j: PV(j), QK(j+1); S_t is therefore overwritten by
-    // QK(j+1) only after PV(j) has read the P that aliases it (the products
-    // of one thread complete in issue order).
+  } else if (warp == WARP_QLOAD) {
+    // ------------------------------------------------------------- Q loads
     if (lane == 0) {
-      const int t = warp - WARP_MMA;
-      constexpr uint32_t IDESC_QK = idesc_bf16_f32(BLOCK_M, BLOCK_N, 0, 0);
-      constexpr uint32_t IDESC_PV = idesc_bf16_f32(BLOCK_M, D, 0, 1);
-      const uint32_t tS = tmem + t * 128;
-      const uint32_t tO = tmem + 256 + t * 128;
-      const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ) + t * C::TILE_BYTES, 16, 1024);
-      const uint32_t ring_addr = smem_u32(sRing);
-      // S_t = Q_t K^T: both operands K-major (head dim contiguous), 16 columns per MMA.
-      auto issue_qk = [&](int slot) {
-        const uint64_t k_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
-          umma_ss(tS, q_desc + off, k_desc + off, IDESC_QK, kk > 0 ? 1u : 0u);
-        }
-      };
-      // O_t (+)= P_t V: P from TMEM (bf16 pairs), V MN-major (head dim contiguous), 16 keys per MMA.
-      auto issue_pv = [&](int slot, bool accumulate) {
-        const uint64_t v_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
-#pragma unroll
-        for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
-          umma_ts(tO, tS + kk * 8, v_desc + static_cast<uint64_t>(kk * 16 * 128 >> 4), IDESC_PV,
-                  (accumulate || kk > 0) ? 1u : 0u);
-        }
-      };
-      // A ring slot this tile does not read is still released, after it has
-      // been filled, so both issuers arrive once per fill in fill order.
-      auto release = [&](int slot, bool used) {
-        if (used) umma_commit(empty_bar(slot));
-        else mbar_arrive(empty_bar(slot));
-      };
-      uint32_t it = 0, qcnt = 0, pcnt = 0;
+      uint32_t qfills[NQT] = {0, 0};
       bool ok = true;
       for (int k = 0; k * static_cast<int>(gridDim.x) < num_units && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= num_units) continue;
         Unit w;
         if (!decode_unit(p, u, w)) continue;
-        const int nkv = kv_tiles(p, w, t);
-        const int nmax = max(kv_tiles(p, w, 0), kv_tiles(p, w, 1));
-        if (nmax == 0) continue;
-        if (nkv > 0) {
-          if (!(ok = wait_or_abort(qfull_bar(t), qcnt & 1u, abort_flag, 1))) break;
-          ++qcnt;
-        }
-        // K_0
-        {
-          const int s = it % C::NS;
-          if (!(ok = wait_or_abort(full_bar(s), (it / C::NS) & 1u, abort_flag, 1))) break;
-          tc_fence_after();
-          if (nkv > 0) {
-            issue_qk(s);
-            umma_commit(sfull_bar(t));
-            if (nkv == 1) umma_commit(qempty_bar(t));
-          }
-          release(s, nkv > 0);
-          ++it;
-        }
-        for (int j = 0; j < nmax; ++j) {
-          const int sv = it % C::NS;
-          if (!(ok = wait_or_abort(full_bar(sv), (it / C::NS) & 1u, abort_flag, 1))) break;
-          tc_fence_after();
-          ++it;
-          if (j < nkv) {
-            if (!(ok = wait_or_abort(pfull_bar(t), pcnt & 1u, abort_flag, 1))) break;
-            ++pcnt;
-            tc_fence_after();
-            issue_pv(sv, j > 0);
-            if (j + 1 == nkv) umma_commit(odone_bar(t));  // last PV of this tile in the unit
-          }
-          release(sv, j < nkv);
-          if (j + 1 < nmax) {
-            const int sk = it % C::NS;
-            if (!(ok = wait_or_abort(full_bar(sk), (it / C::NS) & 1u, abort_flag, 1))) break;
-            tc_fence_after();
-            ++it;
-            const bool use_k = j + 1 < nkv;
-            if (use_k) {
-              issue_qk(sk);
-              umma_commit(sfull_bar(t));
-              if (j + 2 == nkv) umma_commit(qempty_bar(t));
-            }
-            release(sk, use_k);
-          }
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (!ok || kv_tiles(p, w, t) == 0) continue;
+          if (!(ok = wait_or_abort(qempty_bar(t), (qfills[t] & 1u) ^ 1u, abort_flag, 4))) continue;
+          mbar_arrive_expect_tx(qfull_bar(t), C::TILE_BYTES);
+          const uint32_t dst = smem_u32(sQ + t * C::TILE_BYTES);
+          for (int c = 0; c < C::CHUNKS; ++c)
+            tma_load_3d(dst + c * C::CHUNK_BYTES, &tm_q, qfull_bar(t), c * 64, w.q_y + w.row0 + t * BLOCK_M,
+                        w.q_z);
+          ++qfills[t];
         }
       }
-      // Every MMA issued so far completes before the CTA may release TMEM.
-      umma_commit(drain_bar);
-      wait_drain(drain_bar, 0, abort_flag, 1);
+#pragma unroll
+      for (int t = 0; t < NQT; ++t)
+        if (qfills[t] > 0) wait_drain(qfull_bar(t), (qfills[t] - 1) & 1u, abort_flag, 4);
     }
+  } else if (warp == WARP_MMA) {
+    // ------------------------------------------------------------------ MMA
+    // Per tile the order is QK(0), then for each j: PV(j), QK(j+1); S_t is
+    // therefore overwritten by QK(j+1) only after PV(j) has read the P that
+    // aliases it (the products of one thread complete in issue order).
+    uint32_t elected;
+    asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(elected));
+    const bool leader = elected != 0;
+    constexpr uint32_t IDESC_QK = idesc_bf16_f32(BLOCK_M, BLOCK_N, 0, 0);
+    constexpr uint32_t IDESC_PV = idesc_bf16_f32(BLOCK_M, D, 0, 1);
+    const uint32_t q_addr = smem_u32(sQ);
+    const uint32_t ring_addr = smem_u32(sRing);
+    // S_t = Q_t K^T: both operands K-major (head dim contiguous), 16 columns per MMA.
+    auto issue_qk = [&](int t, int slot) {
+      const uint64_t q_desc = smem_desc_sw128(q_addr + t * C::TILE_BYTES, 16, 1024);
+      const uint64_t k_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, 16, 1024);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
+        if (leader) umma_ss(tmem + t * 128, q_desc + off, k_desc + off, IDESC_QK, kk > 0 ? 1u : 0u);
+      }
+    };
+    // O_t (+)= P_t V: P from TMEM (bf16 pairs), V MN-major (head dim contiguous), 16 keys per MMA.
+    auto issue_pv = [&](int t, int slot, bool accumulate) {
+      const uint64_t v_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+#pragma unroll
+      for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
+        if (leader)
+          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                  v_desc + static_cast<uint64_t>(kk * 16 * 128 >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+      }
+    };
+    auto commit = [&](uint32_t bar) {
+      if (leader) umma_commit(bar);
+      __syncwarp();
+    };
+    uint32_t it = 0;
+    uint32_t qcnt[NQT] = {0, 0}, pcnt[NQT] = {0, 0};
+    bool ok = true;
+    for (int k = 0; k * static_cast<int>(gridDim.x) < num_units && ok; ++k) {
+      const int u = snake_unit(k);
+      if (u >= num_units) continue;
+      Unit w;
+      if (!decode_unit(p, u, w)) continue;
+      int nkv[NQT];
+      int nmax = 0;
+#pragma unroll
+      for (int t = 0; t < NQT; ++t) {
+        nkv[t] = kv_tiles(p, w, t);
+        nmax = max(nmax, nkv[t]);
+      }
+      if (nmax == 0) continue;
+#pragma unroll
+      for (int t = 0; t < NQT; ++t) {
+        if (!ok || nkv[t] == 0) continue;
+        ok = wait_or_abort(qfull_bar(t), qcnt[t] & 1u, abort_flag, 1);
+        ++qcnt[t];
+      }
+      if (!ok) break;
+      // K_0 for every active tile.
+      {
+        const int s = it % C::NS;
+        if (!(ok = wait_or_abort(full_bar(s), (it / C::NS) & 1u, abort_flag, 1))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (nkv[t] == 0) continue;
+          issue_qk(t, s);
+          commit(sfull_bar(t));
+          if (nkv[t] == 1) commit(qempty_bar(t));
+        }
+        commit(empty_bar(s));
+        ++it;
+      }
+      for (int j = 0; j < nmax && ok; ++j) {
+        const int sv = it % C::NS;
+        if (!(ok = wait_or_abort(full_bar(sv), (it / C::NS) & 1u, abort_flag, 1))) break;
+        tc_fence_after();
+        ++it;
+        const bool has_next = j + 1 < nmax;
+        const int sk = it % C::NS;
+        bool k_ready = false;
+#pragma unroll
+        for (int t = 0; t < NQT; ++t) {
+          if (!ok || j >= nkv[t]) continue;
+          if (!(ok = wait_or_abort(pfull_bar(t), pcnt[t] & 1u, abort_flag, 1))) continue;
+          ++pcnt[t];
+          tc_fence_after();
+          issue_pv(t, sv, j > 0);
+          if (j + 1 == nkv[t]) commit(odone_bar(t));  // last PV of this tile in the unit
+          if (j + 1 < nkv[t]) {
+            if (!k_ready) {
+              if (!(ok = wait_or_abort(full_bar(sk), (it / C::NS) & 1u, abort_flag, 1))) continue;
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_qk(t, sk);
+            commit(sfull_bar(t));
+            if (j + 2 == nkv[t]) commit(qempty_bar(t));
+          }
+        }
+        if (!ok) break;
+        commit(empty_bar(sv));
+        if (has_next) {
+          commit(empty_bar(sk));
+          ++it;
+        }
+      }
+    }
+    // Every MMA issued so far completes before the CTA may release TMEM.
+    commit(drain_bar);
+    wait_drain(drain_bar, 0, abort_flag, 1);
   }
   } else {
     setmaxnreg_inc<REG_SOFTMAX>();
