@@ -74,6 +74,11 @@ static_assert(2 * REG_SOFTMAX + REG_OTHER <= 512, "register split exceeds a sub-
 // choice because P and l always share the same stale max.
 constexpr float TAU = 8.0f;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+// L2 prefetch of the next unit: issued when the producer starts loading the
+// K/V tile PREFETCH_LEAD tiles before the end of the current unit, covering
+// the next unit's Q tiles and its first PREFETCH_KV_TILES K/V tiles.
+constexpr int PREFETCH_LEAD = 6;
+constexpr int PREFETCH_KV_TILES = 3;
 
 // Device status word: bit (1 << role) is set when that role gave up waiting.
 __device__ int g_fa_status;
@@ -278,13 +283,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       uint32_t it = 0;
       bool ok = true;
+      // The next unit's Q tiles and first K/V tiles usually come from DRAM
+      // (another head); warming them into L2 a few K/V tiles before the
+      // current unit ends hides most of that latency at the unit boundary.
+      auto prefetch_next_unit = [&](int k_next) {
+        const int un = snake_unit(k_next);
+        if (k_next * static_cast<int>(gridDim.x) >= num_units || un >= num_units) return;
+        Unit wn;
+        if (!decode_unit(p, un, wn)) return;
+        const int nk0 = kv_tiles(p, wn, 0), nk1 = kv_tiles(p, wn, 1);
+        for (int t = 0; t < NQT; ++t) {
+          if ((t == 0 ? nk0 : nk1) == 0) continue;
+          for (int c = 0; c < C::CHUNKS; ++c)
+            tma_prefetch_l2_3d(&tm_q, c * 64, wn.q_y + wn.row0 + t * BLOCK_M, wn.q_z);
+        }
+        const int nn = min(max(nk0, nk1), PREFETCH_KV_TILES);
+        for (int j = 0; j < nn; ++j)
+          for (int c = 0; c < C::CHUNKS; ++c) {
+            tma_prefetch_l2_3d(&tm_k, c * 64, wn.k_y + j * BLOCK_N, wn.k_z);
+            tma_prefetch_l2_3d(&tm_v, c * 64, wn.k_y + j * BLOCK_N, wn.k_z);
+          }
+      };
       for (int k = 0; k * static_cast<int>(gridDim.x) < num_units && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= num_units) continue;
         Unit w;
         if (!decode_unit(p, u, w)) continue;
         const int nmax = max(kv_tiles(p, w, 0), kv_tiles(p, w, 1));
+        if (nmax <= PREFETCH_LEAD) prefetch_next_unit(k + 1);
         for (int j = 0; j < nmax && ok; ++j) {
+          if (j == nmax - PREFETCH_LEAD) prefetch_next_unit(k + 1);
           for (int kv = 0; kv < 2; ++kv) {
             const int s = it % C::NS;
             if (!(ok = wait_or_abort(empty_bar(s), ((it / C::NS) & 1u) ^ 1u, abort_flag, 0))) break;
@@ -483,11 +511,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const int k0 = j * BLOCK_N;
         const bool need_mask = (k0 + BLOCK_N > w.Lk) || (p.causal && k0 + BLOCK_N - 1 > tile_diag);
+        // Column c of this row is visible iff c <= rel (one compare against a
+        // constant per element).  rel_hi, the warp's largest limit, lets the
+        // exponential loop below skip 32-column chunks no lane can see.
+        int rel_hi = BLOCK_N;
         if (need_mask) {
           const int lim = p.causal ? min(w.Lk - 1, diag) : (w.Lk - 1);
+          const int rel = lim - k0;
+          rel_hi = __reduce_max_sync(0xffffffffu, rel);
 #pragma unroll
           for (int c = 0; c < BLOCK_N; ++c)
-            if (k0 + c > lim) s[c] = NEG_INF;
+            if (c > rel) s[c] = NEG_INF;
         }
         // Row max: 3-input max in 4 independent chains.
         float mx4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
@@ -528,12 +562,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int c0 = 0; c0 < BLOCK_N; c0 += 32) {
           uint32_t pk[16];
+          if (c0 > rel_hi) {  // hidden from every lane of the warp: P = 0
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 x = fma2(make_float2(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nb2);
-            const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            acc[i % 4] = add2(acc[i % 4], e);
-            pk[i] = pack_bf16x2(e.x, e.y);
+            for (int i = 0; i < 16; ++i) pk[i] = 0u;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 x = fma2(make_float2(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nb2);
+              const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              acc[i % 4] = add2(acc[i % 4], e);
+              pk[i] = pack_bf16x2(e.x, e.y);
+            }
           }
           tmem_st16(tS + c0 / 2, pk);
         }

@@ -87,6 +87,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Prefetches one box of a 3-D tensor map into L2 (no shared-memory write and
+// no completion signal).  Same coordinate rules as tma_load_3d.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Tensor Memory
 // ---------------------------------------------------------------------------
