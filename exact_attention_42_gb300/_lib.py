@@ -45,6 +45,8 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_smem_bytes.restype = ci
             L.fa_fwd_threads.argtypes = []
             L.fa_fwd_threads.restype = ci
+            L.fa_debug_fault_injection.argtypes = [ci, ctypes.c_double]
+            L.fa_debug_fault_injection.restype = ci
             _lib = L
     return _lib
 
@@ -69,6 +71,13 @@ def fa_device_status() -> int:
     if st not in (0, 6):
         raise FaError(st, "fa_device_status")
     return bits.value
+
+
+def fa_debug_fault_injection(mode: int, wait_limit_seconds: float = 0.0) -> None:
+    """Test hook: mode 1 makes later launches time out on purpose (see fa.h)."""
+    st = lib().fa_debug_fault_injection(int(mode), float(wait_limit_seconds))
+    if st != 0:
+        raise FaError(st, "fa_debug_fault_injection")
 
 
 def fa_fwd_smem_bytes(d: int) -> int:

@@ -43,6 +43,7 @@
 #include <cstdint>
 #include <cstring>
 #include <cmath>
+#include <atomic>
 #include <mutex>
 
 #include "fa.h"
@@ -73,7 +74,7 @@ static_assert(2 * REG_SOFTMAX + REG_OTHER <= 512, "register split exceeds a sub-
 // so unnormalised probabilities stay below 2^TAU.  O / l is unchanged by the
 // choice because P and l always share the same stale max.
 constexpr float TAU = 8.0f;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // default limit per wait: 2 s
 // L2 prefetch of the next unit: issued when the producer starts loading the
 // K/V tile PREFETCH_LEAD tiles before the end of the current unit, covering
 // the next unit's Q tiles and its first PREFETCH_KV_TILES K/V tiles.
@@ -106,6 +107,8 @@ struct Params {
   int causal;
   int nqb;                // dense: query units per head = ceil(Nq / 256)
   int num_units;          // dense: B * Hq * nqb; packed: computed on the device
+  unsigned long long wait_limit_ns;  // bound on every mbarrier wait
+  int fault_inject;       // test hook: 1 = the K/V producer withholds its first fill
 };
 
 struct Unit {
@@ -195,18 +198,19 @@ __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int role) 
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                              int role) {
-  if (mbar_wait(bar, parity, abort_flag, WAIT_LIMIT_NS)) return true;
+                                              int role, uint64_t limit_ns) {
+  if (mbar_wait(bar, parity, abort_flag, limit_ns)) return true;
   if (!*abort_flag) raise_abort(abort_flag, role);
   return false;
 }
 
 // Teardown waits ignore the abort flag: they only wait for copies and MMAs
 // that were already issued, which complete on their own.
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, volatile int* abort_flag, int role) {
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, volatile int* abort_flag, int role,
+                                           uint64_t limit_ns) {
   __shared__ int never;
   never = 0;
-  if (!mbar_wait(bar, parity, &never, WAIT_LIMIT_NS)) raise_abort(abort_flag, role);
+  if (!mbar_wait(bar, parity, &never, limit_ns)) raise_abort(abort_flag, role);
 }
 
 template <int D>
@@ -315,7 +319,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (j == nmax - PREFETCH_LEAD) prefetch_next_unit(k + 1);
           for (int kv = 0; kv < 2; ++kv) {
             const int s = it % C::NS;
-            if (!(ok = wait_or_abort(empty_bar(s), ((it / C::NS) & 1u) ^ 1u, abort_flag, 0))) break;
+            if (!(ok = wait_or_abort(empty_bar(s), ((it / C::NS) & 1u) ^ 1u, abort_flag, 0, p.wait_limit_ns))) break;
+            if (p.fault_inject == 1 && it == 0) {  // test hook: this fill never arrives
+              ++it;
+              continue;
+            }
             mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
             const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
             for (int c = 0; c < C::CHUNKS; ++c)
@@ -329,7 +337,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int s = 0; s < C::NS; ++s) {
         if (it > static_cast<uint32_t>(s)) {
           const uint32_t f = s + C::NS * ((it - 1 - s) / C::NS);
-          wait_drain(full_bar(s), (f / C::NS) & 1u, abort_flag, 0);
+          wait_drain(full_bar(s), (f / C::NS) & 1u, abort_flag, 0, p.wait_limit_ns);
         }
       }
     }
@@ -346,7 +354,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
           if (!ok || kv_tiles(p, w, t) == 0) continue;
-          if (!(ok = wait_or_abort(qempty_bar(t), (qfills[t] & 1u) ^ 1u, abort_flag, 4))) continue;
+          if (!(ok = wait_or_abort(qempty_bar(t), (qfills[t] & 1u) ^ 1u, abort_flag, 4, p.wait_limit_ns))) continue;
           mbar_arrive_expect_tx(qfull_bar(t), C::TILE_BYTES);
           const uint32_t dst = smem_u32(sQ + t * C::TILE_BYTES);
           for (int c = 0; c < C::CHUNKS; ++c)
@@ -357,7 +365,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
 #pragma unroll
       for (int t = 0; t < NQT; ++t)
-        if (qfills[t] > 0) wait_drain(qfull_bar(t), (qfills[t] - 1) & 1u, abort_flag, 4);
+        if (qfills[t] > 0) wait_drain(qfull_bar(t), (qfills[t] - 1) & 1u, abort_flag, 4, p.wait_limit_ns);
     }
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------------ MMA
@@ -414,14 +422,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
       for (int t = 0; t < NQT; ++t) {
         if (!ok || nkv[t] == 0) continue;
-        ok = wait_or_abort(qfull_bar(t), qcnt[t] & 1u, abort_flag, 1);
+        ok = wait_or_abort(qfull_bar(t), qcnt[t] & 1u, abort_flag, 1, p.wait_limit_ns);
         ++qcnt[t];
       }
       if (!ok) break;
       // K_0 for every active tile.
       {
         const int s = it % C::NS;
-        if (!(ok = wait_or_abort(full_bar(s), (it / C::NS) & 1u, abort_flag, 1))) break;
+        if (!(ok = wait_or_abort(full_bar(s), (it / C::NS) & 1u, abort_flag, 1, p.wait_limit_ns))) break;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
@@ -435,7 +443,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       for (int j = 0; j < nmax && ok; ++j) {
         const int sv = it % C::NS;
-        if (!(ok = wait_or_abort(full_bar(sv), (it / C::NS) & 1u, abort_flag, 1))) break;
+        if (!(ok = wait_or_abort(full_bar(sv), (it / C::NS) & 1u, abort_flag, 1, p.wait_limit_ns))) break;
         tc_fence_after();
         ++it;
         const bool has_next = j + 1 < nmax;
@@ -444,14 +452,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
           if (!ok || j >= nkv[t]) continue;
-          if (!(ok = wait_or_abort(pfull_bar(t), pcnt[t] & 1u, abort_flag, 1))) continue;
+          if (!(ok = wait_or_abort(pfull_bar(t), pcnt[t] & 1u, abort_flag, 1, p.wait_limit_ns))) continue;
           ++pcnt[t];
           tc_fence_after();
           issue_pv(t, sv, j > 0);
           if (j + 1 == nkv[t]) commit(odone_bar(t));  // last PV of this tile in the unit
           if (j + 1 < nkv[t]) {
             if (!k_ready) {
-              if (!(ok = wait_or_abort(full_bar(sk), (it / C::NS) & 1u, abort_flag, 1))) continue;
+              if (!(ok = wait_or_abort(full_bar(sk), (it / C::NS) & 1u, abort_flag, 1, p.wait_limit_ns))) continue;
               tc_fence_after();
               k_ready = true;
             }
@@ -470,7 +478,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     // Every MMA issued so far completes before the CTA may release TMEM.
     commit(drain_bar);
-    wait_drain(drain_bar, 0, abort_flag, 1);
+    wait_drain(drain_bar, 0, abort_flag, 1, p.wait_limit_ns);
   }
   } else {
     setmaxnreg_inc<REG_SOFTMAX>();
@@ -499,7 +507,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float m_used = NEG_INF;
       float l = 0.f;
       for (int j = 0; j < nkv; ++j) {
-        if (!(ok = wait_or_abort(sfull_bar(t), scnt & 1u, abort_flag, 2 + t))) break;
+        if (!(ok = wait_or_abort(sfull_bar(t), scnt & 1u, abort_flag, 2 + t, p.wait_limit_ns))) break;
         ++scnt;
         tc_fence_after();
         float s[BLOCK_N];
@@ -589,7 +597,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
       if (nkv > 0) {
-        if (!(ok = wait_or_abort(odone_bar(t), ocnt & 1u, abort_flag, 2 + t))) break;
+        if (!(ok = wait_or_abort(odone_bar(t), ocnt & 1u, abort_flag, 2 + t, p.wait_limit_ns))) break;
         ++ocnt;
         tc_fence_after();
       }
@@ -674,6 +682,10 @@ struct DeviceInfo {
   bool attr_set[2] = {false, false};
 };
 
+// Test hook state (process-wide): see fa_debug_fault_injection.
+static std::atomic<int> g_fault_mode{0};
+static std::atomic<unsigned long long> g_wait_limit_ns{WAIT_LIMIT_NS};
+
 static constexpr int kMaxDevices = 64;
 static DeviceInfo g_dev[kMaxDevices];
 static std::mutex g_dev_mutex;
@@ -741,6 +753,8 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
   prm.group = Hq / Hkv;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.causal = causal ? 1 : 0;
+  prm.wait_limit_ns = g_wait_limit_ns.load();
+  prm.fault_inject = g_fault_mode.load();
   long long grid;
   if (packed) {
     prm.nqb = 0;
@@ -807,6 +821,17 @@ fa_status fa_device_status(int* bits) {
   if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
   *bits = v;
   return v ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds) {
+  if (mode < 0 || mode > 1) return FA_ERR_VALUE;
+  if (!(wait_limit_seconds <= 10.0)) return FA_ERR_VALUE;  // also rejects NaN
+  const unsigned long long ns = wait_limit_seconds > 0.0
+                                    ? static_cast<unsigned long long>(wait_limit_seconds * 1e9)
+                                    : fa::WAIT_LIMIT_NS;
+  fa::g_wait_limit_ns.store(ns);
+  fa::g_fault_mode.store(mode);
+  return FA_OK;
 }
 
 int fa_fwd_smem_bytes(int d) {

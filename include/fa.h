@@ -88,6 +88,18 @@ const char* fa_status_string(fa_status s);
  */
 fa_status fa_device_status(int* bits);
 
+/*
+ * fa_debug_fault_injection -- test hook for the failure path (process-wide,
+ * affects later fa_fwd calls).  mode 0 is normal operation; mode 1 makes the
+ * kernel's K/V producer withhold its first copy, so the bounded waits of the
+ * other roles run out: the kernel then records FA_ERR_TIMEOUT bits in the
+ * device status word, waits for its own copies in flight, frees its Tensor
+ * Memory and exits, leaving the CUDA context usable.  wait_limit_seconds
+ * (0 < x <= 10) sets the bound on every wait inside the kernel; 0 restores the
+ * default of 2 s.  Returns FA_ERR_VALUE for other arguments.
+ */
+fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds);
+
 /* Dynamic shared memory (bytes) and threads per CTA used for head dim d;
  * 0 for an unsupported d.  For tooling and tests. */
 int fa_fwd_smem_bytes(int d);
