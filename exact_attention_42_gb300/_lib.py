@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_threads.restype = ci
             L.fa_debug_fault_injection.argtypes = [ci, ctypes.c_double]
             L.fa_debug_fault_injection.restype = ci
+            L.fa_debug_exp2_soft.argtypes = [vp, vp, ci, vp]
+            L.fa_debug_exp2_soft.restype = ci
             _lib = L
     return _lib
 
@@ -78,6 +80,13 @@ def fa_debug_fault_injection(mode: int, wait_limit_seconds: float = 0.0) -> None
     st = lib().fa_debug_fault_injection(int(mode), float(wait_limit_seconds))
     if st != 0:
         raise FaError(st, "fa_debug_fault_injection")
+
+
+def fa_debug_exp2_soft(x_ptr: int, y_ptr: int, n: int, stream: int = 0) -> None:
+    """Test entry point: the kernel's software 2^x on n device floats."""
+    st = lib().fa_debug_exp2_soft(x_ptr, y_ptr, int(n), stream)
+    if st != 0:
+        raise FaError(st, "fa_debug_exp2_soft")
 
 
 def fa_fwd_smem_bytes(d: int) -> int:

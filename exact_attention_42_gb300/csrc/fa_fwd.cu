@@ -80,6 +80,16 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // default limit per wait: 2 
 // the next unit's Q tiles and its first PREFETCH_KV_TILES K/V tiles.
 constexpr int PREFETCH_LEAD = 6;
 constexpr int PREFETCH_KV_TILES = 3;
+// Software exponentials: in tiles without a mask, one score pair in every
+// SOFT_EXP_PERIOD is exponentiated on the FMA/ALU pipes (exp2_soft2) instead
+// of the MUFU unit; 0 turns this off.  Off by default: on GB300 the MUFU unit
+// runs at about a quarter of its peak in this kernel while the softmax warps
+// are bound by instruction issue, and moving one pair in 4 (3, 2) to the
+// polynomial made the B2/H32/N4096/d128 causal forward 24% (29%, 41%) slower.
+#ifndef FA_SOFT_EXP_PERIOD
+#define FA_SOFT_EXP_PERIOD 0
+#endif
+constexpr int SOFT_EXP_PERIOD = FA_SOFT_EXP_PERIOD;
 
 // Device status word: bit (1 << role) is set when that role gave up waiting.
 __device__ int g_fa_status;
@@ -577,7 +587,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float2 x = fma2(make_float2(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nb2);
-              const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              float2 e;
+              if (SOFT_EXP_PERIOD > 0 && (i % (SOFT_EXP_PERIOD > 0 ? SOFT_EXP_PERIOD : 1)) == SOFT_EXP_PERIOD - 1 &&
+                  !need_mask)
+                e = exp2_soft2(x);  // no -inf here: the tile has no masked score
+              else
+                e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
               acc[i % 4] = add2(acc[i % 4], e);
               pk[i] = pack_bf16x2(e.x, e.y);
             }
@@ -636,6 +651,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+}
+
+// Applies exp2_soft2 to pairs of x (test entry point for its error bound).
+__global__ void exp2_soft_kernel(const float* __restrict__ x, float* __restrict__ y, int n) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i + 1 < n) {
+    const float2 r = exp2_soft2(make_float2(x[i], x[i + 1]));
+    y[i] = r.x;
+    y[i + 1] = r.y;
+  } else if (i < n) {
+    y[i] = exp2_soft2(make_float2(x[i], 0.f)).x;
   }
 }
 
@@ -832,6 +859,15 @@ fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds) {
   fa::g_wait_limit_ns.store(ns);
   fa::g_fault_mode.store(mode);
   return FA_OK;
+}
+
+fa_status fa_debug_exp2_soft(const float* x, float* y, int n, cudaStream_t stream) {
+  if (n < 0) return FA_ERR_SHAPE;
+  if (n == 0) return FA_OK;
+  if (x == nullptr || y == nullptr) return FA_ERR_NULL;
+  const int pairs = (n + 1) / 2;
+  fa::exp2_soft_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(x, y, n);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_fwd_smem_bytes(int d) {

@@ -298,6 +298,39 @@ __device__ __forceinline__ float2 add2(float2 a, float2 b) {
   return r;
 }
 
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+// Software 2^x for two arguments on the FMA/ALU pipes (no MUFU).
+// Range reduction x = k + f with k = round(x), f in [-1/2, 1/2]: adding
+// 1.5 * 2^23 rounds x to an integer held in the low mantissa bits of t; then
+// 2^f comes from a degree-3 polynomial and 2^k is added to the exponent bits.
+// The coefficients are the minimax fit for relative error on [-1/2, 1/2]
+// from gen_exp2_poly.py (Remez exchange); maximum relative error 7.5e-5.
+// Arguments below -125 are clamped (result ~2^-125 instead of ~0) so the
+// exponent add cannot wrap; callers keep -inf away from this function.
+__device__ __forceinline__ float2 exp2_soft2(float2 x) {
+  constexpr float MAGIC = 12582912.0f;  // 1.5 * 2^23
+  constexpr float C0 = 0x1.fff692p-1f, C1 = 0x1.62f31ap-1f, C2 = 0x1.f0de1ap-3f, C3 = 0x1.c3f760p-5f;
+  x.x = fmaxf(x.x, -125.0f);
+  x.y = fmaxf(x.y, -125.0f);
+  const float2 t = add2(x, make_float2(MAGIC, MAGIC));
+  const float2 f = sub2(x, sub2(t, make_float2(MAGIC, MAGIC)));
+  float2 q = fma2(make_float2(C3, C3), f, make_float2(C2, C2));
+  q = fma2(q, f, make_float2(C1, C1));
+  q = fma2(q, f, make_float2(C0, C0));
+  // The bit pattern of MAGIC has nine zero low bits, so (bits(t) << 23) is k << 23.
+  return make_float2(__int_as_float(__float_as_int(q.x) + (__float_as_int(t.x) << 23)),
+                     __int_as_float(__float_as_int(q.y) + (__float_as_int(t.y) << 23)));
+}
+
 // Three-input maximum.
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float r;

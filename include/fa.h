@@ -100,6 +100,16 @@ fa_status fa_device_status(int* bits);
  */
 fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds);
 
+/*
+ * fa_debug_exp2_soft -- test entry point: y[i] = 2^x[i] computed by the
+ * kernel's software exponential (FMA/ALU pipes only), for n device floats,
+ * asynchronously on `stream`.  Range reduction 2^x = 2^k * 2^f with k = round(x),
+ * then a degree-3 minimax polynomial for 2^f on [-1/2, 1/2]; maximum relative
+ * error 7.5e-5 for -125 <= x <= 8.  Arguments below -125 give about 2^-125.
+ * (The "software exp" of the interview canvas, element v4-card-body.)
+ */
+fa_status fa_debug_exp2_soft(const float* x, float* y, int n, cudaStream_t stream);
+
 /* Dynamic shared memory (bytes) and threads per CTA used for head dim d;
  * 0 for an unsupported d.  For tooling and tests. */
 int fa_fwd_smem_bytes(int d);

@@ -186,3 +186,22 @@ def test_host_entry_matches_device_entry(fa, dev):
     o_h, l_h = fa.fwd_host(qh, kh, vh, causal=True)
     o_d, l_d = fa.fwd(qh.to(dev), kh.to(dev), vh.to(dev), causal=True)
     assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+
+
+def test_software_exp2_error_bound(fa, dev):
+    """The FMA-pipe 2^x used for part of the exponentials: relative error below
+    the minimax bound of its polynomial (7.5e-5, a little slack for rounding)."""
+    x = torch.cat([torch.linspace(-125.0, 8.0, 1 << 20, dtype=torch.float32),
+                   torch.tensor([0.0, 0.5, -0.5, 1.0, -1.0, 7.75, -124.5, -125.0], dtype=torch.float32)]).to(dev)
+    y = torch.empty_like(x)
+    fa.fa_debug_exp2_soft(x.data_ptr(), y.data_ptr(), x.numel(), torch.cuda.current_stream(dev).cuda_stream)
+    torch.cuda.synchronize(dev)
+    xe = x.double().cpu()
+    rel = ((y.double().cpu() - torch.exp2(xe)) / torch.exp2(xe)).abs()
+    assert float(rel.max()) < 8e-5, float(rel.max())
+    # Arguments below the clamp stay tiny and positive (never wrap negative or to inf).
+    z = torch.tensor([-126.0, -300.0, -1e30], dtype=torch.float32, device=dev)
+    w = torch.empty_like(z)
+    fa.fa_debug_exp2_soft(z.data_ptr(), w.data_ptr(), 3, torch.cuda.current_stream(dev).cuda_stream)
+    torch.cuda.synchronize(dev)
+    assert bool(((w > 0) & (w < 1e-37)).all())
