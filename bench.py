@@ -373,9 +373,15 @@ def run_ours(args):
     peaks = load_peaks()
     achieved = flops / (ms_total / args.steps * 1e-3) / 1e12
     tag = "of measured" if peaks["source"] == "measured" else "of fallback"
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops"], "traffic": load_traffic(name),
-                "peak_kind": "bf16 dense burst " + tag,
+    # A timed region of a second or more runs under the power cap, like the
+    # seconds-long GEMM loop behind the sustained peak; shorter runs compare
+    # against the burst peak.
+    sustained = ms_total >= 1000.0
+    peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": load_traffic(name),
+                "peak_kind": "bf16 dense %s %s" % ("sustained" if sustained else "burst", tag),
+                "frac_of_burst": achieved / peaks["bf16_tflops"],
                 "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                 "kernel": "fa_fwd_kernel", "algorithmic_flop_per_launch": flops,
                 "algorithmic_bytes_per_launch": prob.io_bytes()}
