@@ -34,7 +34,11 @@ if ROOT not in sys.path:
 METRIC = "attention fwd TFLOP/s bf16 (N=4096,d=128,causal) and % of dense-BF16 peak"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["exact_attention_42_gb300/csrc/fa_fwd.cu", "exact_attention_42_gb300/csrc/ptx.cuh"]
+KERNEL_SOURCES = {
+    "fa_fwd_kernel": ["exact_attention_42_gb300/csrc/fa_fwd.cu", "exact_attention_42_gb300/csrc/ptx.cuh"],
+    "decode_kernel": ["exact_attention_42_gb300/csrc/fa_decode.cu", "exact_attention_42_gb300/csrc/fa_internal.h",
+                      "exact_attention_42_gb300/csrc/ptx.cuh"],
+}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 ROTATE = 3            # input copies cycled through, so each step reads from HBM
 L2_BYTES = 129 * 2 ** 20
@@ -56,9 +60,10 @@ def parse_args(argv=None):
 
 # ---------------------------------------------------------------- helpers
 
-def kernel_hash() -> str:
+def kernel_hash(kernel: str = "fa_fwd_kernel") -> str:
+    """Digest of the sources one kernel is built from (ties ncu figures to them)."""
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -89,7 +94,7 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def load_traffic(workload: str):
+def load_traffic(workload: str, kernel: str = "fa_fwd_kernel"):
     """ncu DRAM bytes per launch, if captured for this exact kernel source."""
     try:
         with open(TRAFFIC_FILE) as f:
@@ -97,7 +102,7 @@ def load_traffic(workload: str):
     except (OSError, ValueError):
         return None
     e = d.get(workload)
-    if not e or e.get("kernel_sha") != kernel_hash():
+    if not e or e.get("kernel_sha") != kernel_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -180,6 +185,11 @@ def barrier(world: int, device=None):
             dist.barrier(device_ids=[device.index])
         else:
             dist.barrier()
+
+
+def is_decode(prob) -> bool:
+    """Whether fa_fwd runs this problem on the split-KV (decode) path."""
+    return (not prob.varlen) and prob.Nk > 0 and (prob.Hq // prob.Hkv) * prob.Nq <= 16
 
 
 def workload_config(prob, name):
@@ -371,20 +381,29 @@ def run_ours(args):
     e2e_value = world * flops / (e2e_ms * 1e-3) / 1e12
 
     peaks = load_peaks()
-    achieved = flops / (ms_total / args.steps * 1e-3) / 1e12
     tag = "of measured" if peaks["source"] == "measured" else "of fallback"
-    # A timed region of a second or more runs under the power cap, like the
-    # seconds-long GEMM loop behind the sustained peak; shorter runs compare
-    # against the burst peak.
-    sustained = ms_total >= 1000.0
-    peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": load_traffic(name),
-                "peak_kind": "bf16 dense %s %s" % ("sustained" if sustained else "burst", tag),
-                "frac_of_burst": achieved / peaks["bf16_tflops"],
-                "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                "kernel": "fa_fwd_kernel", "algorithmic_flop_per_launch": flops,
-                "algorithmic_bytes_per_launch": prob.io_bytes()}
+    launch_s = ms_total / args.steps * 1e-3
+    if is_decode(prob):
+        # Split-KV path: bound by reading K and V from HBM.
+        achieved = prob.io_bytes() / launch_s / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"], "traffic": load_traffic(name, "decode_kernel"),
+                    "peak_kind": "HBM copy bandwidth " + tag, "kernel": "decode_kernel",
+                    "algorithmic_bytes_per_launch": prob.io_bytes(), "algorithmic_flop_per_launch": flops}
+    else:
+        achieved = flops / launch_s / 1e12
+        # A timed region of a second or more runs under the power cap, like the
+        # seconds-long GEMM loop behind the sustained peak; shorter runs compare
+        # against the burst peak.
+        sustained = ms_total >= 1000.0
+        peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": load_traffic(name),
+                    "peak_kind": "bf16 dense %s %s" % ("sustained" if sustained else "burst", tag),
+                    "frac_of_burst": achieved / peaks["bf16_tflops"],
+                    "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                    "kernel": "fa_fwd_kernel", "algorithmic_flop_per_launch": flops,
+                    "algorithmic_bytes_per_launch": prob.io_bytes()}
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -397,7 +416,7 @@ def run_ours(args):
             "gpu_launches": args.steps,
             "clocks": clocks,
             "device_status": status_bits,
-            "kernel_sha": kernel_hash()}
+            "kernel_sha": kernel_hash(roofline["kernel"])}
     if rank == 0 and not args.no_cpu_baseline:
         v_cpu, threads, desc, _ = oracle_sample(prob, args.cpu_budget_s)
         line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}

@@ -49,6 +49,10 @@ def lib() -> ctypes.CDLL:
             L.fa_debug_fault_injection.restype = ci
             L.fa_debug_exp2_soft.argtypes = [vp, vp, ci, vp]
             L.fa_debug_exp2_soft.restype = ci
+            L.fa_decode.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, ci, vp]
+            L.fa_decode.restype = ci
+            L.fa_decode_smem_bytes.argtypes = [ci]
+            L.fa_decode_smem_bytes.restype = ci
             _lib = L
     return _lib
 
@@ -57,6 +61,11 @@ def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens, st
     """Direct call of the C entry point with integer addresses; returns the status."""
     return lib().fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, ctypes.c_float(scale), int(causal),
                         cu_seqlens, stream)
+
+
+def fa_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream) -> int:
+    """Direct call of the split-KV entry point with integer addresses; returns the status."""
+    return lib().fa_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, ctypes.c_float(scale), int(causal), stream)
 
 
 def fa_status_string(status: int) -> str:

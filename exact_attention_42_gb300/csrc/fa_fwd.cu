@@ -47,6 +47,7 @@
 #include <mutex>
 
 #include "fa.h"
+#include "fa_internal.h"
 #include "ptx.cuh"
 
 namespace fa {
@@ -688,18 +689,22 @@ static EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [heads, rows, d] bf16 tensor, loaded as 128-row x 64-column boxes with the
+// [heads, rows, d] bf16 tensor, loaded as box_rows x 64-column boxes with the
 // 128-byte swizzle that the UMMA K-major / MN-major descriptors expect.
-static bool encode_rows_map(CUtensorMap* map, const void* base, int d, long long rows, long long heads) {
+bool encode_bf16_rows_map(CUtensorMap* map, const void* base, int d, long long rows, long long heads, int box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
-  cuuint32_t box[3] = {64, BLOCK_M, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t elem[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, elem,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool encode_rows_map(CUtensorMap* map, const void* base, int d, long long rows, long long heads) {
+  return encode_bf16_rows_map(map, base, d, rows, heads, BLOCK_M);
 }
 
 struct DeviceInfo {
@@ -744,6 +749,9 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
   DeviceInfo* di = nullptr;
   fa_status st = device_info(dev, &di);
   if (st != FA_OK) return st;
+  if (decode_supported(B, Hq, Hkv, Nq, Nk, D, cu_seqlens))
+    return launch_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, stream, di->sms,
+                         g_wait_limit_ns.load());
   {
     std::lock_guard<std::mutex> lock(g_dev_mutex);
     const int idx = (D == 128) ? 1 : 0;
@@ -846,9 +854,34 @@ fa_status fa_device_status(int* bits) {
   if (cudaMemcpyFromSymbol(&v, fa::g_fa_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
   const int zero = 0;
   if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  const int dv = fa::decode_status_and_clear();
+  if (dv < 0) return FA_ERR_CUDA;
+  if (dv) v |= 1 << 8;  // the split-KV kernel gave up on a wait
   *bits = v;
   return v ? FA_ERR_TIMEOUT : FA_OK;
 }
+
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
+                    int Nk, int d, float scale, int causal, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
+  if (Hq % Hkv != 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_VALUE;
+  if (B == 0 || Hq == 0 || Nq == 0) return FA_OK;
+  if (!fa::decode_supported(B, Hq, Hkv, Nq, Nk, d, nullptr)) return FA_ERR_UNSUPPORTED;
+  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr) return FA_ERR_NULL;
+  auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+  if (mis16(q) || mis16(k) || mis16(v) || mis16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  fa::DeviceInfo* di = nullptr;
+  const fa_status st = fa::device_info(dev, &di);
+  if (st != FA_OK) return st;
+  return fa::launch_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream, di->sms,
+                           fa::g_wait_limit_ns.load());
+}
+
+int fa_decode_smem_bytes(int d) { return fa::decode_smem_bytes(d); }
 
 fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds) {
   if (mode < 0 || mode > 1) return FA_ERR_VALUE;

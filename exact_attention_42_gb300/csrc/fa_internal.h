@@ -1,0 +1,26 @@
+// Host-side declarations shared by the translation units of libfa.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "fa.h"
+
+namespace fa {
+
+constexpr int kMaxDevicesDecode = 64;
+
+// Tensor map of a [heads, rows, d] bf16 tensor read in boxes of 64 columns x
+// box_rows rows with the 128-byte swizzle; false if the driver rejects it.
+bool encode_bf16_rows_map(CUtensorMap* map, const void* base, int d, long long rows, long long heads, int box_rows);
+
+// Split-KV path (fa_decode.cu) for dense problems with (Hq / Hkv) * Nq <= 16.
+bool decode_supported(int B, int Hq, int Hkv, int Nq, int Nk, int d, const int32_t* cu_seqlens);
+fa_status launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream, int sms,
+                        unsigned long long wait_limit_ns);
+int decode_status_and_clear();  // -1 if the status word cannot be read
+int decode_smem_bytes(int d);
+
+}  // namespace fa

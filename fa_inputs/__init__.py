@@ -216,6 +216,11 @@ WORKLOADS = {
     "gqa_b1_hq32_hkv8_n16384_d128_causal": dict(kind="dense", B=1, Hq=32, Hkv=8, Nq=16384, Nk=16384, d=128,
                                                 seed=4, causal=True, k_outlier_frac=0.01),
     "varlen16_h16_d128_causal": dict(kind="varlen", H=16, d=128, seed=5, causal=True),
+    # Decode (split-KV path): a few new tokens per sequence against a long context.
+    "decode_b8_hq32_hkv8_nq1_nk32768_d128": dict(kind="dense", B=8, Hq=32, Hkv=8, Nq=1, Nk=32768, d=128, seed=6,
+                                                 causal=False),
+    "decode_b16_hq32_hkv8_nq4_nk8192_d128_causal": dict(kind="dense", B=16, Hq=32, Hkv=8, Nq=4, Nk=8192, d=128,
+                                                        seed=7, causal=True),
 }
 
 HEADLINE = "b2_h32_n4096_d128_causal"

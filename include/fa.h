@@ -76,13 +76,33 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
                  const int32_t* cu_seqlens, cudaStream_t stream);
 
+/*
+ * fa_decode -- the same computation as fa_fwd (dense layout only) by the
+ * split-KV path for few query rows per key/value head: it requires
+ * (Hq / Hkv) * Nq <= 16 and Nk >= 1, and returns FA_ERR_UNSUPPORTED otherwise.
+ * fa_fwd itself takes this path for such dense problems.  Work is bound by
+ * reading K and V once from HBM, since every new token reads all earlier
+ * tokens' K/V (KV-cache overview canvas, element text-0023).  One thread-block
+ * cluster per (batch, key/value head) splits the keys over up to 8 CTAs.
+ * Their partial (max, sum, output)
+ * states are merged through distributed shared memory (m* = max m_s,
+ * l* = sum l_s e^(m_s - m*), O* = sum O_s e^(m_s - m*) / l*), so no scratch
+ * memory is used.  Arguments, layouts, ownership and errors are as for
+ * fa_fwd; the call is asynchronous on `stream`.
+ */
+fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse,
+                    int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                    cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* fa_status_string(fa_status s);
 
 /*
- * fa_device_status -- reads and clears the device status word of the current
+ * fa_device_status -- reads and clears the device status words of the current
  * device.  Every wait inside the kernels is bounded; a wait that runs out sets
- * a bit in this word and the kernel leaves cleanly.  Returns FA_OK and stores
+ * a bit and the kernel leaves cleanly.  Bits 0-4: roles of the fa_fwd kernel
+ * (K/V producer, MMA issuer, softmax of query tiles 0 and 1, Q loader);
+ * bit 8: the split-KV kernel.  Returns FA_OK and stores
  * 0 in *bits when nothing went wrong, FA_ERR_TIMEOUT with the bits otherwise.
  * This call synchronises the device (it reads device memory).
  */
@@ -114,6 +134,7 @@ fa_status fa_debug_exp2_soft(const float* x, float* y, int n, cudaStream_t strea
  * 0 for an unsupported d.  For tooling and tests. */
 int fa_fwd_smem_bytes(int d);
 int fa_fwd_threads(void);
+int fa_decode_smem_bytes(int d);
 
 #ifdef __cplusplus
 }
