@@ -53,6 +53,11 @@ def lib() -> ctypes.CDLL:
             L.fa_decode.restype = ci
             L.fa_decode_smem_bytes.argtypes = [ci]
             L.fa_decode_smem_bytes.restype = ci
+            L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, ci,
+                                 vp, vp]
+            L.fa_bwd.restype = ci
+            L.fa_bwd_smem_bytes.argtypes = [ci]
+            L.fa_bwd_smem_bytes.restype = ci
             _lib = L
     return _lib
 
@@ -66,6 +71,13 @@ def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens, st
 def fa_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream) -> int:
     """Direct call of the split-KV entry point with integer addresses; returns the status."""
     return lib().fa_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, ctypes.c_float(scale), int(causal), stream)
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens,
+           stream) -> int:
+    """Direct call of the backward entry point with integer addresses; returns the status."""
+    return lib().fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, d, ctypes.c_float(scale),
+                        int(causal), cu_seqlens, stream)
 
 
 def fa_status_string(status: int) -> str:
@@ -104,3 +116,7 @@ def fa_fwd_smem_bytes(d: int) -> int:
 
 def fa_fwd_threads() -> int:
     return lib().fa_fwd_threads()
+
+
+def fa_bwd_smem_bytes(d: int) -> int:
+    return lib().fa_bwd_smem_bytes(d)

@@ -10,7 +10,7 @@ from typing import Optional, Tuple
 
 import torch
 
-from ._lib import FaError, fa_fwd
+from ._lib import FaError, fa_bwd, fa_fwd
 
 
 def _check(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int, device) -> None:
@@ -101,3 +101,42 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
     lh.copy_(lse, non_blocking=nb)
     torch.cuda.current_stream(device).synchronize()
     return oh, lh
+
+
+def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
+        dout: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
+        stream: Optional[torch.cuda.Stream] = None):
+    """Gradients of exact attention on the GPU; returns (dQ, dK, dV, delta).
+
+    Dense layout only: q, o, dout [B, Hq, Nq, d], k/v [B, Hkv, Nk, d] bf16,
+    lse [B, Hq, Nq] fp32 from ``fwd`` on the same inputs.  delta [B, Hq, Nq]
+    fp32 is rowsum(dout * o).  Runs on ``stream`` (default: the current
+    stream) without synchronising.
+    """
+    dev = q.device
+    _check(q, "q", torch.bfloat16, 4, None)
+    for t, n in ((k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
+        _check(t, n, torch.bfloat16, 4, dev)
+    _check(lse, "lse", torch.float32, 3, dev)
+    B, Hq, Nq, d = q.shape
+    Bk, Hkv, Nk, dk_ = k.shape
+    if Bk != B or dk_ != d or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("k and v must be [B, Hkv, Nk, d] with q's B and d")
+    if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("o and dout must have q's shape")
+    if tuple(lse.shape) != (B, Hq, Nq):
+        raise ValueError("lse must be [B, Hq, Nq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    delta = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                    dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), B, Hq, Hkv, Nq, Nk, d,
+                    float(scale), int(bool(causal)), None, s.cuda_stream)
+    if st != 0:
+        raise FaError(st, "fa_bwd")
+    return dq, dk, dv, delta

@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG_DIR, "libfa.so")
-SOURCES = [os.path.join(CSRC, "fa_fwd.cu"), os.path.join(CSRC, "fa_decode.cu")]
+SOURCES = [os.path.join(CSRC, "fa_fwd.cu"), os.path.join(CSRC, "fa_decode.cu"), os.path.join(CSRC, "fa_bwd.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "fa_internal.h"), os.path.join(INCLUDE, "fa.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,0 +1,917 @@
+// Exact attention backward for GB300 (sm_103a).
+//
+// What it computes: the gradients of O = softmax(scale Q K^T) V for an
+// upstream gradient dO.  The forward pass keeps only O and one statistic per
+// row (its LSE); the backward pass recomputes the scores and probabilities
+// tile by tile instead of reading a stored N x N matrix ("FlashAttention面试讲解"
+// interview canvas, elements v1-card-body and qa3-a).  Per head, with
+// P = exp(S - LSE) recomputed from the stored LSE:
+//   dV = P^T dO,  dP = dO V^T,  D_i = dO_i . O_i,  dS = P (dP - D),
+//   dQ = scale dS K,  dK = scale dS^T Q.
+// Under grouped-query attention the dK and dV of a key/value head sum over
+// its query heads.
+//
+// Three kernels, none of which uses scratch memory or atomics:
+//   bwd_delta_kernel  D = rowsum(dO * O) (fp32, one value per query row; an
+//                     output of the call, like LSE in the forward pass)
+//   bwd_dq_kernel     query-stationary: a CTA owns 128 query rows and walks
+//                     the K/V tiles: S = Q K^T and dP = dO V^T into TMEM,
+//                     dS (bf16) back into TMEM, dQ += dS K as a TS product.
+//                     The next tile's S and dP are issued as soon as the
+//                     softmax warps have read the current ones, so the
+//                     exponentials overlap the tensor pipe.
+//   bwd_dkdv_kernel   key-stationary: a CTA owns 128 keys and walks the query
+//                     tiles of every query head that reads them:
+//                     S^T = K Q^T and dP^T = V dO^T into TMEM, P^T and dS^T
+//                     (bf16) back into TMEM, then dV += P^T dO and
+//                     dK += dS^T Q as TS products.
+// The score products are computed twice (once per kernel), seven products
+// per tile pair instead of five; in exchange dQ needs no cross-CTA
+// reduction, so results are deterministic and no workspace is needed.
+//
+// CTA layout of both main kernels (320 threads, one persistent CTA per SM):
+//   warps 0-3  softmax warpgroup 0: columns [0, 64) of every 128-wide tile
+//   warps 4-7  softmax warpgroup 1: columns [64, 128); thread r of each
+//              warpgroup owns TMEM lane r (a query row, or a key row)
+//   warp 8     TMA producer (one lane)
+//   warp 9     MMA issuer and TMEM owner (whole warp, one elected lane)
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <cstring>
+#include <cmath>
+
+#include "fa.h"
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace bwd {
+
+constexpr int TILE = 128;          // rows per Q, dO, K or V tile (= TMEM lanes)
+constexpr int NUM_THREADS = 320;
+constexpr int WARP_PRODUCER = 8;
+constexpr int WARP_MMA = 9;
+constexpr int SOFTMAX_THREADS = 256;
+constexpr float LOG2E = 1.4426950408889634f;
+
+// Device status word: bit (1 << role) is set when that role gave up waiting.
+// dQ kernel: 0 producer, 1 MMA, 2 softmax; dK/dV kernel: 4, 5, 6.
+__device__ int g_bwd_status;
+
+template <int D>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int TILE_BYTES = TILE * D * 2;
+  static constexpr int CHUNKS = D / 64;
+  static constexpr int CHUNK_BYTES = TILE * 128;
+  static constexpr int NS = (D == 128) ? 4 : 8;  // ring slots
+  static constexpr int SMEM_FIXED = 2 * TILE_BYTES;  // Q + dO (dQ kernel) or K + V (dK/dV kernel)
+  static constexpr int SMEM_RING = NS * TILE_BYTES;
+  static constexpr int SMEM_VEC = 2 * 2 * TILE * 4;  // dK/dV kernel: LSE and D of two query tiles
+  static constexpr int NUM_BARS = 2 * NS + 12;
+  static constexpr int SMEM_BYTES = 1024 + SMEM_FIXED + SMEM_RING + SMEM_VEC + NUM_BARS * 8 + 16;
+};
+
+struct Params {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* dout;
+  const __nv_bfloat16* o;
+  const float* lse;
+  float* delta;
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int B, Hq, Hkv, Nq, Nk, group;
+  float scale;
+  float scale_log2;  // scale * log2(e)
+  int causal;
+  int nqt, nkt;      // query / key tiles per head
+  int num_units;
+  unsigned long long wait_limit_ns;
+};
+
+__device__ __forceinline__ void raise_abort(volatile int* abort_flag, int role) {
+  *abort_flag = 1;
+  atomicOr(&g_bwd_status, 1 << role);
+}
+
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag, int role,
+                                              uint64_t limit_ns) {
+  if (mbar_wait(bar, parity, abort_flag, limit_ns)) return true;
+  if (!*abort_flag) raise_abort(abort_flag, role);
+  return false;
+}
+
+// Teardown waits ignore the abort flag: they wait only for copies and
+// products already issued, which complete on their own.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, volatile int* abort_flag, int role,
+                                           uint64_t limit_ns, volatile int* never) {
+  if (!mbar_wait(bar, parity, never, limit_ns)) raise_abort(abort_flag, role);
+}
+
+__device__ __forceinline__ uint32_t elect_leader() {
+  uint32_t elected;
+  asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(elected));
+  return elected;
+}
+
+// Static "snake" schedule over units (the forward kernel's): round k gives
+// CTA c unit k*G + c for even k and k*G + G-1-c for odd k.
+__device__ __forceinline__ int snake_unit(int k) {
+  const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return k * g + ((k & 1) ? (g - 1 - c) : c);
+}
+
+// ---------------------------------------------------------------------------
+// D = rowsum(dO * O): D/8 threads per row, one 16-byte load of each per thread
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const __nv_bfloat16* __restrict__ dout,
+                                                        float* __restrict__ delta, long long rows) {
+  constexpr int TPR = D / 8;
+  const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = t / TPR;
+  const int part = static_cast<int>(t % TPR);
+  float acc = 0.f;
+  if (row < rows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(o + row * D + part * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(dout + row * D + part * 8);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(bw[i] << 16), acc);
+      acc = fmaf(__uint_as_float(aw[i] & 0xFFFF0000u), __uint_as_float(bw[i] & 0xFFFF0000u), acc);
+    }
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && part == 0) delta[row] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// dQ: query-stationary
+// TMEM: [0,128) S   [128,256) dP   [256,256+D) dQ   [384,448) [448,512) dS x2
+// ---------------------------------------------------------------------------
+
+// Unit u -> (batch*head, query tile); heavier (later) query tiles first under
+// a causal mask.
+__device__ __forceinline__ void dq_unit(const Params& p, int u, int& bh, int& qt) {
+  const int bh_count = p.B * p.Hq;
+  qt = p.nqt - 1 - u / bh_count;
+  bh = u % bh_count;
+}
+
+// K/V tiles query tile qt must visit (0: no key visible to any of its rows).
+__device__ __forceinline__ int dq_kv_tiles(const Params& p, int qt) {
+  const int q0 = qt * TILE;
+  if (q0 >= p.Nq || p.Nk <= 0) return 0;
+  int last_key = p.Nk - 1;
+  if (p.causal) {
+    last_key = min(last_key, min(q0 + TILE - 1, p.Nq - 1) + (p.Nk - p.Nq));
+    if (last_key < 0) return 0;
+  }
+  return last_key / TILE + 1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + C::TILE_BYTES;
+  uint8_t* sRing = smem + C::SMEM_FIXED;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + C::SMEM_RING + C::SMEM_VEC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* never = abort_flag + 1;
+
+  const uint32_t bar_base = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (C::NS + s); };
+  const uint32_t qfull_bar = bar_base + 8u * (2 * C::NS + 0);
+  const uint32_t qempty_bar = bar_base + 8u * (2 * C::NS + 1);
+  const uint32_t sdp_full_bar = bar_base + 8u * (2 * C::NS + 2);
+  const uint32_t sdp_free_bar = bar_base + 8u * (2 * C::NS + 3);
+  const uint32_t ds_full_bar = bar_base + 8u * (2 * C::NS + 4);
+  auto ds_free_bar = [&](int b) { return bar_base + 8u * (2 * C::NS + 5 + b); };
+  const uint32_t dq_done_bar = bar_base + 8u * (2 * C::NS + 7);
+  const uint32_t dq_free_bar = bar_base + 8u * (2 * C::NS + 8);
+  const uint32_t drain_bar = bar_base + 8u * (2 * C::NS + 9);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(qfull_bar, 1);
+    mbar_init(qempty_bar, 1);
+    mbar_init(sdp_full_bar, 1);
+    mbar_init(sdp_free_bar, SOFTMAX_THREADS);
+    mbar_init(ds_full_bar, SOFTMAX_THREADS);
+    mbar_init(ds_free_bar(0), 1);
+    mbar_init(ds_free_bar(1), 1);
+    mbar_init(dq_done_bar, 1);
+    mbar_init(dq_free_bar, SOFTMAX_THREADS);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *never = 0;
+    fence_mbar_init();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int num_units = p.num_units;
+  const int nrounds = (num_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+
+  if (warp == WARP_PRODUCER) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      if (p.Nk > 0) {  // with no keys the K/V maps are left unencoded and never used
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+      }
+      uint32_t it = 0, qfills = 0;
+      bool ok = true;
+      for (int k = 0; k < nrounds && ok; ++k) {
+        const int u = snake_unit(k);
+        if (u >= num_units) continue;
+        int bh, qt;
+        dq_unit(p, u, bh, qt);
+        const int nkv = dq_kv_tiles(p, qt);
+        if (nkv == 0) continue;
+        const int b = bh / p.Hq, kvz = b * p.Hkv + (bh % p.Hq) / p.group;
+        if (!(ok = wait_or_abort(qempty_bar, (qfills & 1u) ^ 1u, abort_flag, 0, p.wait_limit_ns))) break;
+        mbar_arrive_expect_tx(qfull_bar, 2 * C::TILE_BYTES);
+        for (int c = 0; c < C::CHUNKS; ++c) {
+          tma_load_3d(smem_u32(sQ) + c * C::CHUNK_BYTES, &tm_q, qfull_bar, c * 64, qt * TILE, bh);
+          tma_load_3d(smem_u32(sDO) + c * C::CHUNK_BYTES, &tm_do, qfull_bar, c * 64, qt * TILE, bh);
+        }
+        ++qfills;
+        for (int j = 0; j < nkv && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int s = it % C::NS;
+            if (!(ok = wait_or_abort(empty_bar(s), ((it / C::NS) & 1u) ^ 1u, abort_flag, 0, p.wait_limit_ns)))
+              break;
+            mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
+            const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, full_bar(s), c * 64, j * TILE, kvz);
+            ++it;
+          }
+        }
+      }
+      // Every issued copy lands before the CTA may exit.
+      for (int s = 0; s < C::NS; ++s) {
+        if (it > static_cast<uint32_t>(s)) {
+          const uint32_t f = s + C::NS * ((it - 1 - s) / C::NS);
+          wait_drain(full_bar(s), (f / C::NS) & 1u, abort_flag, 0, p.wait_limit_ns, never);
+        }
+      }
+      if (qfills > 0) wait_drain(qfull_bar, (qfills - 1) & 1u, abort_flag, 0, p.wait_limit_ns, never);
+    }
+  } else if (warp == WARP_MMA) {
+    const bool leader = elect_leader() != 0;
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(TILE, TILE, 0, 0);
+    constexpr uint32_t IDESC_DQ = idesc_bf16_f32(TILE, D, 0, 1);
+    const uint32_t ring_addr = smem_u32(sRing);
+    const uint64_t q_desc = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+    const uint64_t do_desc = smem_desc_sw128(smem_u32(sDO), 16, 1024);
+    auto commit = [&](uint32_t bar) {
+      if (leader) umma_commit(bar);
+      __syncwarp();
+    };
+    uint32_t it = 0, gt = 0, units_done = 0, qcnt = 0;
+    bool ok = true;
+    for (int k = 0; k < nrounds && ok; ++k) {
+      const int u = snake_unit(k);
+      if (u >= num_units) continue;
+      int bh, qt;
+      dq_unit(p, u, bh, qt);
+      const int nkv = dq_kv_tiles(p, qt);
+      if (nkv == 0) continue;
+      if (!(ok = wait_or_abort(qfull_bar, qcnt & 1u, abort_flag, 1, p.wait_limit_ns))) break;
+      ++qcnt;
+      const uint32_t it0 = it;
+      // S(g) = Q K_j^T and dP(g) = dO V_j^T for the unit's tile j (global
+      // tile g).  K_j sits in ring fill it0 + 2j, V_j in it0 + 2j + 1.  The
+      // S/dP columns are reused once the softmax warps have read tile g-1.
+      auto sdp = [&](int j) -> bool {
+        const uint32_t g = gt + j;
+        if (g > 0 && !wait_or_abort(sdp_free_bar, (g - 1) & 1u, abort_flag, 1, p.wait_limit_ns)) return false;
+        const uint32_t fk = it0 + 2 * j, fv = fk + 1;
+        if (!wait_or_abort(full_bar(fk % C::NS), (fk / C::NS) & 1u, abort_flag, 1, p.wait_limit_ns)) return false;
+        tc_fence_after();
+        const uint64_t k_desc = smem_desc_sw128(ring_addr + (fk % C::NS) * C::TILE_BYTES, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
+          if (leader) umma_ss(tmem + 0, q_desc + off, k_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        if (!wait_or_abort(full_bar(fv % C::NS), (fv / C::NS) & 1u, abort_flag, 1, p.wait_limit_ns)) return false;
+        tc_fence_after();
+        const uint64_t v_desc = smem_desc_sw128(ring_addr + (fv % C::NS) * C::TILE_BYTES, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
+          if (leader) umma_ss(tmem + 128, do_desc + off, v_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        commit(sdp_full_bar);
+        commit(empty_bar(fv % C::NS));  // V_j is read only by dP
+        if (j == nkv - 1) commit(qempty_bar);
+        return true;
+      };
+      if (!(ok = sdp(0))) break;
+      for (int j = 0; j < nkv && ok; ++j) {
+        const uint32_t g = gt + j;
+        if (j + 1 < nkv && !(ok = sdp(j + 1))) break;
+        if (!(ok = wait_or_abort(ds_full_bar, g & 1u, abort_flag, 1, p.wait_limit_ns))) break;
+        if (j == 0 && units_done > 0 &&
+            !(ok = wait_or_abort(dq_free_bar, (units_done - 1) & 1u, abort_flag, 1, p.wait_limit_ns)))
+          break;
+        tc_fence_after();
+        const uint32_t fk = it0 + 2 * j;
+        const uint64_t kmn_desc = smem_desc_sw128(ring_addr + (fk % C::NS) * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+        const uint32_t ds_col = 384 + 64 * (g & 1u);
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk) {
+          if (leader)
+            umma_ts(tmem + 256, tmem + ds_col + kk * 8, kmn_desc + static_cast<uint64_t>(kk * 16 * 128 >> 4),
+                    IDESC_DQ, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        commit(ds_free_bar(g & 1u));
+        commit(empty_bar(fk % C::NS));
+        if (j == nkv - 1) commit(dq_done_bar);
+      }
+      if (!ok) break;
+      it = it0 + 2 * nkv;
+      gt += nkv;
+      ++units_done;
+    }
+    commit(drain_bar);
+    wait_drain(drain_bar, 0, abort_flag, 1, p.wait_limit_ns, never);
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int h = warp / 4;  // column half
+    const int r = threadIdx.x % 128;
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + 64 * h;
+    const uint32_t tDP = tmem + lane_base + 128 + 64 * h;
+    const uint32_t tDQ = tmem + lane_base + 256 + (D / 2) * h;
+    const float sl2 = p.scale_log2;
+    uint32_t gt = 0, units_done = 0;
+    bool ok = true;
+    for (int k = 0; k < nrounds && ok; ++k) {
+      const int u = snake_unit(k);
+      if (u >= num_units) continue;
+      int bh, qt;
+      dq_unit(p, u, bh, qt);
+      const int nkv = dq_kv_tiles(p, qt);
+      const int row = qt * TILE + r;
+      const bool row_ok = row < p.Nq;
+      const long long grow = static_cast<long long>(bh) * p.Nq + row;
+      if (nkv == 0) {
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dq + grow * D + (D / 2) * h);
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
+      const float lse2 = row_ok ? __ldg(p.lse + grow) * LOG2E : INFINITY;
+      const float dlt = row_ok ? __ldg(p.delta + grow) : 0.f;
+      const int lim = row_ok ? (p.causal ? min(p.Nk - 1, row + (p.Nk - p.Nq)) : (p.Nk - 1)) : -1;
+      for (int j = 0; j < nkv; ++j) {
+        const uint32_t g = gt + j;
+        if (!(ok = wait_or_abort(sdp_full_bar, g & 1u, abort_flag, 2, p.wait_limit_ns))) break;
+        tc_fence_after();
+        uint32_t sr[64], dpr[64];
+        tmem_ld64_wait(tS, sr);
+        tmem_ld64_wait(tDP, dpr);
+        tc_fence_before();
+        mbar_arrive(sdp_free_bar);
+        const int rel = lim - (j * TILE + 64 * h);  // columns c <= rel are visible
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float ds2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = 2 * i + e;
+            const float pr = (c <= rel) ? ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2)) : 0.f;
+            ds2[e] = pr * (__uint_as_float(dpr[c]) - dlt);
+          }
+          pk[i] = pack_bf16x2(ds2[0], ds2[1]);
+        }
+        if (g >= 2 && !(ok = wait_or_abort(ds_free_bar(g & 1u), ((g >> 1) - 1) & 1u, abort_flag, 2, p.wait_limit_ns)))
+          break;
+        tc_fence_after();
+        tmem_st32(tmem + lane_base + 384 + 64 * (g & 1u) + 32 * h, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(ds_full_bar);
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ epilogue
+      if (!(ok = wait_or_abort(dq_done_bar, units_done & 1u, abort_flag, 2, p.wait_limit_ns))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < D / 2; c0 += 32) {
+        uint32_t raw[32];
+        tmem_ld32_wait(tDQ + c0, raw);
+        uint32_t out[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          out[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * p.scale, __uint_as_float(raw[2 * i + 1]) * p.scale);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dq + grow * D + (D / 2) * h + c0);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free_bar);
+      gt += nkv;
+      ++units_done;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dK, dV: key-stationary
+// TMEM: [0,128) S^T   [128,256) dP^T   [256,256+D) dV   [384,384+D) dK
+// P^T (bf16 pairs) overwrites S^T columns [64h, 64h+32) and dS^T overwrites
+// dP^T columns [128+64h, 128+64h+32): each softmax warpgroup writes only
+// over scores it has already read.
+// ---------------------------------------------------------------------------
+
+// Unit u -> (batch*kv head, key tile); under a causal mask the first key
+// tiles are read by the most query tiles, so they come first.
+__device__ __forceinline__ void kv_unit(const Params& p, int u, int& bkv, int& kt) {
+  const int n = p.B * p.Hkv;
+  kt = u / n;
+  bkv = u % n;
+}
+
+// First query tile that sees any key of key tile kt (nqt: none).
+__device__ __forceinline__ int kv_first_qtile(const Params& p, int kt) {
+  if (!p.causal) return 0;
+  const int q_min = kt * TILE - (p.Nk - p.Nq);  // first query row whose diagonal reaches key kt*TILE
+  if (q_min <= 0) return 0;
+  if (q_min >= p.Nq) return p.nqt;
+  return q_min / TILE;
+}
+
+template <int D>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem =
+      reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + C::TILE_BYTES;
+  uint8_t* sRing = smem + C::SMEM_FIXED;
+  float* sVec = reinterpret_cast<float*>(sRing + C::SMEM_RING);  // [2][LSE*log2e (128), D (128)]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + C::SMEM_RING + C::SMEM_VEC);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* never = abort_flag + 1;
+
+  const uint32_t bar_base = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar_base + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_base + 8u * (C::NS + s); };
+  const uint32_t kvfull_bar = bar_base + 8u * (2 * C::NS + 0);
+  const uint32_t kvempty_bar = bar_base + 8u * (2 * C::NS + 1);
+  const uint32_t sdp_full_bar = bar_base + 8u * (2 * C::NS + 2);
+  const uint32_t pds_full_bar = bar_base + 8u * (2 * C::NS + 3);
+  const uint32_t dkv_done_bar = bar_base + 8u * (2 * C::NS + 4);
+  const uint32_t dkv_free_bar = bar_base + 8u * (2 * C::NS + 5);
+  const uint32_t drain_bar = bar_base + 8u * (2 * C::NS + 6);
+  // The LSE / D vectors of query tile g are in buffer g % 2; vec_bar(g % 2)
+  // completes when all softmax threads have written their entry.
+  auto vec_bar = [&](int b) { return bar_base + 8u * (2 * C::NS + 7 + b); };
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    mbar_init(vec_bar(0), SOFTMAX_THREADS);
+    mbar_init(vec_bar(1), SOFTMAX_THREADS);
+    mbar_init(kvfull_bar, 1);
+    mbar_init(kvempty_bar, 1);
+    mbar_init(sdp_full_bar, 1);
+    mbar_init(pds_full_bar, SOFTMAX_THREADS);
+    mbar_init(dkv_done_bar, 1);
+    mbar_init(dkv_free_bar, SOFTMAX_THREADS);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *never = 0;
+    fence_mbar_init();
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int num_units = p.num_units;
+  const int nrounds = (num_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+
+  if (warp == WARP_PRODUCER) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_do);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      uint32_t it = 0, kvfills = 0;
+      bool ok = true;
+      for (int k = 0; k < nrounds && ok; ++k) {
+        const int u = snake_unit(k);
+        if (u >= num_units) continue;
+        int bkv, kt;
+        kv_unit(p, u, bkv, kt);
+        const int i0 = kv_first_qtile(p, kt);
+        if (i0 >= p.nqt) continue;
+        if (!(ok = wait_or_abort(kvempty_bar, (kvfills & 1u) ^ 1u, abort_flag, 4, p.wait_limit_ns))) break;
+        mbar_arrive_expect_tx(kvfull_bar, 2 * C::TILE_BYTES);
+        for (int c = 0; c < C::CHUNKS; ++c) {
+          tma_load_3d(smem_u32(sK) + c * C::CHUNK_BYTES, &tm_k, kvfull_bar, c * 64, kt * TILE, bkv);
+          tma_load_3d(smem_u32(sV) + c * C::CHUNK_BYTES, &tm_v, kvfull_bar, c * 64, kt * TILE, bkv);
+        }
+        ++kvfills;
+        const int b = bkv / p.Hkv, kvh = bkv % p.Hkv;
+        for (int hg = 0; hg < p.group && ok; ++hg) {
+          const int qz = b * p.Hq + kvh * p.group + hg;
+          for (int i = i0; i < p.nqt && ok; ++i) {
+            for (int x = 0; x < 2; ++x) {
+              const int s = it % C::NS;
+              if (!(ok = wait_or_abort(empty_bar(s), ((it / C::NS) & 1u) ^ 1u, abort_flag, 4, p.wait_limit_ns)))
+                break;
+              mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
+              const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
+              for (int c = 0; c < C::CHUNKS; ++c)
+                tma_load_3d(dst + c * C::CHUNK_BYTES, x ? &tm_do : &tm_q, full_bar(s), c * 64, i * TILE, qz);
+              ++it;
+            }
+          }
+        }
+      }
+      for (int s = 0; s < C::NS; ++s) {
+        if (it > static_cast<uint32_t>(s)) {
+          const uint32_t f = s + C::NS * ((it - 1 - s) / C::NS);
+          wait_drain(full_bar(s), (f / C::NS) & 1u, abort_flag, 4, p.wait_limit_ns, never);
+        }
+      }
+      if (kvfills > 0) wait_drain(kvfull_bar, (kvfills - 1) & 1u, abort_flag, 4, p.wait_limit_ns, never);
+    }
+  } else if (warp == WARP_MMA) {
+    const bool leader = elect_leader() != 0;
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(TILE, TILE, 0, 0);
+    constexpr uint32_t IDESC_G = idesc_bf16_f32(TILE, D, 0, 1);
+    const uint32_t ring_addr = smem_u32(sRing);
+    const uint64_t k_desc = smem_desc_sw128(smem_u32(sK), 16, 1024);
+    const uint64_t v_desc = smem_desc_sw128(smem_u32(sV), 16, 1024);
+    auto commit = [&](uint32_t bar) {
+      if (leader) umma_commit(bar);
+      __syncwarp();
+    };
+    uint32_t it = 0, gt = 0, units_done = 0, kvcnt = 0;
+    bool ok = true;
+    for (int k = 0; k < nrounds && ok; ++k) {
+      const int u = snake_unit(k);
+      if (u >= num_units) continue;
+      int bkv, kt;
+      kv_unit(p, u, bkv, kt);
+      const int i0 = kv_first_qtile(p, kt);
+      if (i0 >= p.nqt) continue;
+      const int ntiles = p.group * (p.nqt - i0);
+      if (!(ok = wait_or_abort(kvfull_bar, kvcnt & 1u, abort_flag, 5, p.wait_limit_ns))) break;
+      ++kvcnt;
+      for (int t = 0; t < ntiles && ok; ++t) {
+        const uint32_t g = gt + t;
+        const uint32_t fq = it, fd = it + 1;
+        const int sq = fq % C::NS, sd = fd % C::NS;
+        if (!(ok = wait_or_abort(full_bar(sq), (fq / C::NS) & 1u, abort_flag, 5, p.wait_limit_ns))) break;
+        tc_fence_after();
+        const uint64_t q_desc = smem_desc_sw128(ring_addr + sq * C::TILE_BYTES, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
+          if (leader) umma_ss(tmem + 0, k_desc + off, q_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        if (!(ok = wait_or_abort(full_bar(sd), (fd / C::NS) & 1u, abort_flag, 5, p.wait_limit_ns))) break;
+        tc_fence_after();
+        const uint64_t do_desc = smem_desc_sw128(ring_addr + sd * C::TILE_BYTES, 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
+          if (leader) umma_ss(tmem + 128, v_desc + off, do_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        commit(sdp_full_bar);
+        if (!(ok = wait_or_abort(pds_full_bar, g & 1u, abort_flag, 5, p.wait_limit_ns))) break;
+        if (t == 0 && units_done > 0 &&
+            !(ok = wait_or_abort(dkv_free_bar, (units_done - 1) & 1u, abort_flag, 5, p.wait_limit_ns)))
+          break;
+        tc_fence_after();
+        const uint64_t do_mn = smem_desc_sw128(ring_addr + sd * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+        const uint64_t q_mn = smem_desc_sw128(ring_addr + sq * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk) {
+          const uint32_t acol = 64 * (kk / 4) + 8 * (kk % 4);  // query pairs of warpgroup kk/4
+          const uint64_t boff = static_cast<uint64_t>(kk * 16 * 128) >> 4;
+          if (leader) {
+            umma_ts(tmem + 256, tmem + acol, do_mn + boff, IDESC_G, (t > 0 || kk > 0) ? 1u : 0u);
+            umma_ts(tmem + 384, tmem + 128 + acol, q_mn + boff, IDESC_G, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        commit(empty_bar(sq));
+        commit(empty_bar(sd));
+        it += 2;
+      }
+      if (!ok) break;
+      commit(dkv_done_bar);
+      commit(kvempty_bar);
+      gt += ntiles;
+      ++units_done;
+    }
+    commit(drain_bar);
+    wait_drain(drain_bar, 0, abort_flag, 5, p.wait_limit_ns, never);
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int h = warp / 4;  // query-column half
+    const int r = threadIdx.x % 128;
+    const int tt = threadIdx.x;  // 0..255: loader index of the LSE / D vectors
+    const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + 64 * h;
+    const uint32_t tDP = tmem + lane_base + 128 + 64 * h;
+    const float sl2 = p.scale_log2;
+    const int shift = p.Nk - p.Nq;
+    uint32_t gt = 0, units_done = 0;
+    bool ok = true;
+    for (int k = 0; k < nrounds && ok; ++k) {
+      const int u = snake_unit(k);
+      if (u >= num_units) continue;
+      int bkv, kt;
+      kv_unit(p, u, bkv, kt);
+      const int i0 = kv_first_qtile(p, kt);
+      const int key = kt * TILE + r;
+      const bool key_ok = key < p.Nk;
+      const long long krow = static_cast<long long>(bkv) * p.Nk + key;
+      if (i0 >= p.nqt) {
+        if (key_ok) {
+          uint4* dk = reinterpret_cast<uint4*>(p.dk + krow * D + (D / 2) * h);
+          uint4* dv = reinterpret_cast<uint4*>(p.dv + krow * D + (D / 2) * h);
+#pragma unroll
+          for (int i = 0; i < D / 16; ++i) dk[i] = dv[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
+      const int b = bkv / p.Hkv, kvh = bkv % p.Hkv;
+      const int per_head = p.nqt - i0;
+      const int ntiles = p.group * per_head;
+      // Tile t covers query head kvh*group + t/per_head, query tile i0 + t%per_head.
+      auto vec_value = [&](int t) -> float {
+        const int qh = kvh * p.group + t / per_head;
+        const int q = (i0 + t % per_head) * TILE + (tt & 127);
+        const long long qrow = (static_cast<long long>(b) * p.Hq + qh) * p.Nq + q;
+        if (tt < 128) return q < p.Nq ? __ldg(p.lse + qrow) * LOG2E : INFINITY;
+        return q < p.Nq ? __ldg(p.delta + qrow) : 0.f;
+      };
+      float v_next = vec_value(0);
+      for (int t = 0; t < ntiles; ++t) {
+        const uint32_t g = gt + t;
+        // Buffer g % 2 was last read in tile g - 2; every thread has passed
+        // vec_bar of tile g - 1 since, which it reached only after that.
+        float* vec = sVec + (g & 1u) * 256;
+        vec[tt] = v_next;
+        mbar_arrive(vec_bar(g & 1u));
+        if (t + 1 < ntiles) v_next = vec_value(t + 1);
+        if (!(ok = wait_or_abort(vec_bar(g & 1u), (g >> 1) & 1u, abort_flag, 6, p.wait_limit_ns))) break;
+        if (!(ok = wait_or_abort(sdp_full_bar, g & 1u, abort_flag, 6, p.wait_limit_ns))) break;
+        tc_fence_after();
+        const int q0 = (i0 + t % per_head) * TILE + 64 * h;
+        // Query column c is visible to this key iff the query exists
+        // (c <= qmax) and, under the causal mask, the key is on or left of
+        // the query's diagonal (c >= cmin).
+        const int qmax = p.Nq - 1 - q0;
+        const int cmin = p.causal ? key - shift - q0 : -0x40000000;
+        // Two halves of 32 columns; each half's P^T / dS^T (16 packed
+        // columns) lands over scores already read.
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t sr[32], dpr[32];
+          tmem_ld32_wait(tS + 32 * half, sr);
+          tmem_ld32_wait(tDP + 32 * half, dpr);
+          uint32_t ppk[16], dpk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float pr[2], ds[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = 32 * half + 2 * i + e;
+              const bool vis = key_ok && c <= qmax && c >= cmin;
+              pr[e] = vis ? ex2_approx(fmaf(__uint_as_float(sr[2 * i + e]), sl2, -vec[64 * h + c])) : 0.f;
+              ds[e] = pr[e] * (__uint_as_float(dpr[2 * i + e]) - vec[128 + 64 * h + c]);
+            }
+            ppk[i] = pack_bf16x2(pr[0], pr[1]);
+            dpk[i] = pack_bf16x2(ds[0], ds[1]);
+          }
+          tmem_st16(tS + 16 * half, ppk);
+          tmem_st16(tDP + 16 * half, dpk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(pds_full_bar);
+      }
+      if (!ok) break;
+      // ------------------------------------------------------------ epilogue
+      if (!(ok = wait_or_abort(dkv_done_bar, units_done & 1u, abort_flag, 6, p.wait_limit_ns))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t tsrc = tmem + lane_base + (which ? 384 : 256) + (D / 2) * h;
+        const float mul = which ? p.scale : 1.f;
+        __nv_bfloat16* base = (which ? p.dk : p.dv) + krow * D + (D / 2) * h;
+#pragma unroll
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t raw[32];
+          tmem_ld32_wait(tsrc + c0, raw);
+          uint32_t out[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            out[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * mul, __uint_as_float(raw[2 * i + 1]) * mul);
+          if (key_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(base + c0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dkv_free_bar);
+      gt += ntiles;
+      ++units_done;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace bwd
+}  // namespace fa
+
+// ============================================================================
+// Host side
+// ============================================================================
+namespace fa {
+
+int bwd_status_and_clear() {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, bwd::g_bwd_status, sizeof(int)) != cudaSuccess) return -1;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(bwd::g_bwd_status, &zero, sizeof(int)) != cudaSuccess) return -1;
+  return v;
+}
+
+int bwd_smem_bytes(int d) {
+  if (d == 64) return bwd::Cfg<64>::SMEM_BYTES;
+  if (d == 128) return bwd::Cfg<128>::SMEM_BYTES;
+  return 0;
+}
+
+template <int D>
+static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                              const float* lse, void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv,
+                              int Nq, int Nk, float scale, int causal, cudaStream_t stream, int sms,
+                              unsigned long long wait_limit_ns) {
+  using C = bwd::Cfg<D>;
+  static bool attr_set[kMaxDevicesDecode] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev >= 0 && dev < kMaxDevicesDecode && !attr_set[dev]) {
+    if (cudaFuncSetAttribute(bwd::bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(bwd::bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::SMEM_BYTES) != cudaSuccess)
+      return FA_ERR_CUDA;
+    attr_set[dev] = true;
+  }
+  // D = rowsum(dO * O) first: both main kernels read it.
+  const long long rows = static_cast<long long>(B) * Hq * Nq;
+  {
+    const long long threads = rows * (D / 8);
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffffLL) return FA_ERR_SHAPE;
+    bwd::bwd_delta_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, rows);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  }
+  alignas(64) CUtensorMap tq, tdo, tk, tv;
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  if (!encode_bf16_rows_map(&tq, q, D, Nq, static_cast<long long>(B) * Hq, bwd::TILE) ||
+      !encode_bf16_rows_map(&tdo, dout, D, Nq, static_cast<long long>(B) * Hq, bwd::TILE))
+    return FA_ERR_CUDA;
+  if (Nk > 0 && (!encode_bf16_rows_map(&tk, k, D, Nk, static_cast<long long>(B) * Hkv, bwd::TILE) ||
+                 !encode_bf16_rows_map(&tv, v, D, Nk, static_cast<long long>(B) * Hkv, bwd::TILE)))
+    return FA_ERR_CUDA;
+  bwd::Params prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.dout = static_cast<const __nv_bfloat16*>(dout);
+  prm.o = static_cast<const __nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.delta = delta;
+  prm.dq = static_cast<__nv_bfloat16*>(dq);
+  prm.dk = static_cast<__nv_bfloat16*>(dk);
+  prm.dv = static_cast<__nv_bfloat16*>(dv);
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Nq = Nq;
+  prm.Nk = Nk;
+  prm.group = Hq / Hkv;
+  prm.scale = scale;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.causal = causal ? 1 : 0;
+  prm.nqt = (Nq + bwd::TILE - 1) / bwd::TILE;
+  prm.nkt = (Nk + bwd::TILE - 1) / bwd::TILE;
+  prm.wait_limit_ns = wait_limit_ns;
+  // dQ: one unit per (batch, query head, query tile).
+  {
+    const long long units = static_cast<long long>(B) * Hq * prm.nqt;
+    if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
+    prm.num_units = static_cast<int>(units);
+    const long long grid = units < sms ? units : sms;
+    if (grid > 0) {
+      bwd::bwd_dq_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, C::SMEM_BYTES, stream>>>(tq, tdo, tk,
+                                                                                                       tv, prm);
+      if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    }
+  }
+  // dK, dV: one unit per (batch, key/value head, key tile).
+  {
+    const long long units = static_cast<long long>(B) * Hkv * prm.nkt;
+    if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
+    prm.num_units = static_cast<int>(units);
+    const long long grid = units < sms ? units : sms;
+    if (grid > 0) {
+      bwd::bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, C::SMEM_BYTES, stream>>>(
+          tq, tdo, tk, tv, prm);
+      if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    }
+  }
+  return FA_OK;
+}
+
+fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                     float scale, int causal, cudaStream_t stream, int sms, unsigned long long wait_limit_ns) {
+  if (d == 128)
+    return launch_bwd_t<128>(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, scale, causal, stream,
+                             sms, wait_limit_ns);
+  return launch_bwd_t<64>(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, scale, causal, stream, sms,
+                          wait_limit_ns);
+}
+
+}  // namespace fa

@@ -857,6 +857,9 @@ fa_status fa_device_status(int* bits) {
   const int dv = fa::decode_status_and_clear();
   if (dv < 0) return FA_ERR_CUDA;
   if (dv) v |= 1 << 8;  // the split-KV kernel gave up on a wait
+  const int bv = fa::bwd_status_and_clear();
+  if (bv < 0) return FA_ERR_CUDA;
+  v |= bv << 9;  // backward kernels: roles 0-2 (dQ) and 4-6 (dK/dV)
   *bits = v;
   return v ? FA_ERR_TIMEOUT : FA_OK;
 }
@@ -882,6 +885,35 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
 }
 
 int fa_decode_smem_bytes(int d) { return fa::decode_smem_bytes(d); }
+
+int fa_bwd_smem_bytes(int d) { return fa::bwd_smem_bytes(d); }
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                 float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
+  if (Hq % Hkv != 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (cu_seqlens != nullptr) return FA_ERR_UNSUPPORTED;
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_VALUE;
+  if (B == 0 || Hq == 0 || Nq == 0) return FA_OK;
+  if (q == nullptr || o == nullptr || dout == nullptr || lse == nullptr || dq == nullptr || delta == nullptr)
+    return FA_ERR_NULL;
+  if (Nk > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr)) return FA_ERR_NULL;
+  auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+  if (mis16(q) || mis16(o) || mis16(dout) || mis16(dq)) return FA_ERR_ALIGN;
+  if (Nk > 0 && (mis16(k) || mis16(v) || mis16(dk) || mis16(dv))) return FA_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || (reinterpret_cast<uintptr_t>(delta) & 3u) != 0)
+    return FA_ERR_ALIGN;
+  if (static_cast<long long>(B) * Hq > 0x7fffffffLL) return FA_ERR_SHAPE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  fa::DeviceInfo* di = nullptr;
+  const fa_status st = fa::device_info(dev, &di);
+  if (st != FA_OK) return st;
+  return fa::launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream,
+                        di->sms, fa::g_wait_limit_ns.load());
+}
 
 fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds) {
   if (mode < 0 || mode > 1) return FA_ERR_VALUE;

@@ -203,6 +203,11 @@ def make_varlen(seqlens, Hq, Hkv, d, seed, causal, scale=None, name="varlen") ->
     return Problem(name, q, k, v, len(seqlens), Hq, Hkv, L, L, d, bool(causal), float(scale), cu)
 
 
+def make_dout(prob: Problem, seed: int) -> np.ndarray:
+    """Upstream gradient dO for the backward pass: bf16 N(0, 1), O's shape."""
+    return normal_bf16(stream_key(seed, 6), prob.q.shape)
+
+
 def varlen_lengths(seed: int, count: int = 16, lo: int = 256, hi: int = 8192):
     return [int(x) for x in uniform_ints(stream_key(seed, 5), count, lo, hi)]
 

@@ -94,6 +94,40 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
                     int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
                     cudaStream_t stream);
 
+/*
+ * fa_bwd -- gradients of the attention forward (dense layout), on `stream`.
+ *
+ * The forward pass keeps only O and the per-row LSE; this call recomputes the
+ * scores and probabilities tile by tile from them instead of reading a stored
+ * N x N matrix ("FlashAttention面试讲解" interview canvas, elements
+ * v1-card-body and qa3-a).  With P = exp(scale Q K^T - LSE) (masked entries 0):
+ *   dV = P^T dO,  dP = dO V^T,  delta_i = dO_i . O_i,  dS = P (dP - delta),
+ *   dQ = scale dS K,  dK = scale dS^T Q,
+ * and under grouped-query attention dK, dV of a key/value head are summed over
+ * its Hq / Hkv query heads.  Masks and conventions are those of fa_fwd.
+ *
+ * Inputs (device, row-major, contiguous):
+ *   q, o, dout [B, Hq, Nq, d] bf16     k, v [B, Hkv, Nk, d] bf16
+ *   lse        [B, Hq, Nq]    fp32     (as written by fa_fwd for the same q, k, v)
+ * Outputs (device, caller-allocated):
+ *   dq [B, Hq, Nq, d] bf16, dk and dv [B, Hkv, Nk, d] bf16,
+ *   delta [B, Hq, Nq] fp32: the per-row statistic rowsum(dout * o).
+ * cu_seqlens must be NULL: the packed layout is not supported by the backward
+ * pass (FA_ERR_UNSUPPORTED).
+ *
+ * Three kernels are enqueued (delta, then dQ, then dK/dV); the library
+ * allocates nothing and uses no atomics, so results are deterministic.
+ * Empty problems (B, Hq or Nq equal to 0) return FA_OK; with Nk == 0, dq and
+ * delta are written (zeros and rowsum(dout * o)) and k, v, dk, dv may be NULL.
+ * Errors are reported as for fa_fwd; argument errors leave every output
+ * untouched.  Device-side time-outs set bits 9-11 (dQ kernel) and 13-15
+ * (dK/dV kernel) of fa_device_status().
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, float* delta,
+                 int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                 const int32_t* cu_seqlens, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* fa_status_string(fa_status s);
 
@@ -102,7 +136,8 @@ const char* fa_status_string(fa_status s);
  * device.  Every wait inside the kernels is bounded; a wait that runs out sets
  * a bit and the kernel leaves cleanly.  Bits 0-4: roles of the fa_fwd kernel
  * (K/V producer, MMA issuer, softmax of query tiles 0 and 1, Q loader);
- * bit 8: the split-KV kernel.  Returns FA_OK and stores
+ * bit 8: the split-KV kernel; bits 9-11 and 13-15: producer, MMA issuer and
+ * softmax roles of fa_bwd's dQ and dK/dV kernels.  Returns FA_OK and stores
  * 0 in *bits when nothing went wrong, FA_ERR_TIMEOUT with the bits otherwise.
  * This call synchronises the device (it reads device memory).
  */
@@ -135,6 +170,7 @@ fa_status fa_debug_exp2_soft(const float* x, float* y, int n, cudaStream_t strea
 int fa_fwd_smem_bytes(int d);
 int fa_fwd_threads(void);
 int fa_decode_smem_bytes(int d);
+int fa_bwd_smem_bytes(int d);
 
 #ifdef __cplusplus
 }
