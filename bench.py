@@ -6,7 +6,12 @@ LSE) over the whole workload, i.e. one launch of the library's kernel.  The
 default workload is B=2, H=32, N=4096, d=128, causal.  FLOPs per step are
 4*B*H*Nq*Nk*d, halved for causal.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+With --bwd a step is instead one backward pass (dQ, dK, dV and delta from
+Q, K, V, O, LSE and dO: three kernel launches); FLOPs per step are counted
+as 2.5 times the forward's (the five products of the plain gradient), so the
+products the kernels recompute are not credited.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--bwd]
     python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
 
 With N > 1 (torchrun), every rank runs its own copy of the workload: the
@@ -32,12 +37,14 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOP/s bf16 (N=4096,d=128,causal) and % of dense-BF16 peak"
+METRIC_BWD = "attention bwd TFLOP/s bf16 (dQ, dK, dV; 2.5x the forward FLOPs) and % of dense-BF16 peak"
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["exact_attention_42_gb300/csrc/fa_fwd.cu", "exact_attention_42_gb300/csrc/ptx.cuh"],
     "decode_kernel": ["exact_attention_42_gb300/csrc/fa_decode.cu", "exact_attention_42_gb300/csrc/fa_internal.h",
                       "exact_attention_42_gb300/csrc/ptx.cuh"],
+    "fa_bwd": ["exact_attention_42_gb300/csrc/fa_bwd.cu", "exact_attention_42_gb300/csrc/ptx.cuh"],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 ROTATE = 3            # input copies cycled through, so each step reads from HBM
@@ -55,6 +62,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--bwd", action="store_true", help="time the backward pass instead of the forward")
     return ap.parse_args(argv)
 
 
@@ -203,13 +211,15 @@ def workload_config(prob, name):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_sample(prob, budget_s: float, start_head: int = 0):
+def oracle_sample(prob, budget_s: float, start_head: int = 0, backward: bool = False):
     """Times the fp64 oracle, as it stands, on whole heads of the workload
     until `budget_s` is spent (at least one head).  Returns (TFLOP/s, threads,
-    description)."""
+    description).  With `backward`, the oracle's gradients of each head (dense
+    workloads), counted at 2.5 times the forward FLOPs."""
     import numpy as np
-    from fa_inputs import bf16_bits_to_f64
-    from oracle import attention_fwd, oracle_threads
+    from fa_inputs import bf16_bits_to_f64, make_dout
+    from oracle import attention_bwd, attention_fwd, oracle_threads
+    dout = make_dout(prob, 1000) if backward else None
 
     flops = 0.0
     heads = 0
@@ -234,14 +244,19 @@ def oracle_sample(prob, budget_s: float, start_head: int = 0):
             k = bf16_bits_to_f64(prob.k[b:b + 1, kvh:kvh + 1])
             v = bf16_bits_to_f64(prob.v[b:b + 1, kvh:kvh + 1])
             f = 4.0 * prob.Nq * prob.Nk * prob.d * (0.5 if prob.causal else 1.0)
-        attention_fwd(q, k, v, prob.scale, prob.causal)
+        if backward:
+            attention_bwd(q, k, v, bf16_bits_to_f64(dout[b:b + 1, h:h + 1]), prob.scale, prob.causal)
+            f *= 2.5
+        else:
+            attention_fwd(q, k, v, prob.scale, prob.causal)
         flops += f
         heads += 1
         hq += 1
         if time.perf_counter() - t0 >= budget_s:
             break
     dt = time.perf_counter() - t0
-    desc = "%d whole head(s) of %s (every query row of each), fp64, %.1f s" % (heads, prob.name, dt)
+    desc = "%d whole head(s) of %s (every query row of each), fp64%s, %.1f s" % (
+        heads, prob.name, ", backward" if backward else "", dt)
     return flops / dt / 1e12, oracle_threads(), desc, dt
 
 
@@ -253,20 +268,23 @@ def run_reference(args):
     from fa_inputs import make_workload, HEADLINE
     name = args.workload or HEADLINE
     prob = make_workload(name)
+    if args.bwd and prob.varlen:
+        raise SystemExit("--bwd: dense workloads only")
     per_step = max(1.0, args.cpu_budget_s / max(1, args.steps))
     for w in range(args.warmup):
-        oracle_sample(prob, 0.0, start_head=w)
+        oracle_sample(prob, 0.0, start_head=w, backward=args.bwd)
     vals, secs, descs = [], [], []
     t0 = time.perf_counter()
     threads = None
     for i in range(args.steps):
-        v, threads, desc, dt = oracle_sample(prob, per_step, start_head=i * 7)
+        v, threads, desc, dt = oracle_sample(prob, per_step, start_head=i * 7, backward=args.bwd)
         vals.append(v)
         secs.append(dt)
         descs.append(desc)
     wall = time.perf_counter() - t0
     value = statistics.mean(vals)
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+    line = {"metric": METRIC_BWD if args.bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
@@ -299,26 +317,43 @@ def run_ours(args):
     barrier(world, dev)
     fa.lib()
 
-    from fa_inputs import make_workload, HEADLINE
+    from fa_inputs import make_workload, make_dout, HEADLINE
     name = args.workload or HEADLINE
     prob = make_workload(name)
-    flops = prob.flops()
+    if args.bwd and prob.varlen:
+        raise SystemExit("--bwd: dense workloads only")
+    flops = prob.flops() * (2.5 if args.bwd else 1.0)
 
     def dev_bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
     q0, k0, v0 = dev_bf16(prob.q), dev_bf16(prob.k), dev_bf16(prob.v)
+    do0 = dev_bf16(make_dout(prob, 1000)) if args.bwd else None
     cu = None if prob.cu_seqlens is None else torch.from_numpy(prob.cu_seqlens).to(dev)
     sets = []
     for r in range(ROTATE):
         q, k, v = (q0, k0, v0) if r == 0 else (q0.clone(), k0.clone(), v0.clone())
         o = torch.empty_like(q)
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
-        sets.append((q, k, v, o, lse))
+        if args.bwd:
+            # The forward pass's O and LSE are inputs of the backward step.
+            fa.fwd(q, k, v, causal=prob.causal, scale=prob.scale, out=o, lse=lse)
+            do = do0 if r == 0 else do0.clone()
+            grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                     torch.empty(q.shape[:-1], dtype=torch.float32, device=dev))
+            sets.append((q, k, v, o, lse, do) + grads)
+        else:
+            sets.append((q, k, v, o, lse))
     step_bytes = sum(t.numel() * t.element_size() for t in sets[0])
     stream = torch.cuda.current_stream(dev)
+    launches_per_step = 3 if args.bwd else 1
 
     def step(i):
+        if args.bwd:
+            q, k, v, o, lse, do, dq, dk, dv, dl = sets[i % ROTATE]
+            fa.bwd(q, k, v, o, lse, do, causal=prob.causal, scale=prob.scale, stream=stream,
+                   dq=dq, dk=dk, dv=dv, delta=dl)
+            return
         q, k, v, o, lse = sets[i % ROTATE]
         fa.fwd(q, k, v, causal=prob.causal, scale=prob.scale, cu_seqlens=cu, out=o, lse=lse, stream=stream)
 
@@ -351,21 +386,30 @@ def run_ours(args):
     value = world * flops / (ms_step * 1e-3) / 1e12
 
     # End to end through the public API: pinned host inputs copied in, the
-    # kernel, O and LSE copied back, every step.
-    qh, kh, vh = (t.cpu().pin_memory() for t in (q0, k0, v0))
-    oh = torch.empty(q0.shape, dtype=torch.bfloat16, pin_memory=True)
-    lh = torch.empty(q0.shape[:-1], dtype=torch.float32, pin_memory=True)
-    q, k, v, o, lse = sets[0]
-    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
-    d2h = oh.numel() * 2 + lh.numel() * 4
+    # kernels, the results copied back, every step.
+    if args.bwd:
+        q, k, v, o, lse, do, dq, dk, dv, dl = sets[0]
+        ins = (q, k, v, o, lse, do)
+        outs = (dq, dk, dv, dl)
+    else:
+        q, k, v, o, lse = sets[0]
+        ins = (q, k, v)
+        outs = (o, lse)
+    hins = tuple(t.cpu().pin_memory() for t in ins)
+    houts = tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs)
+    h2d = sum(t.numel() * t.element_size() for t in hins)
+    d2h = sum(t.numel() * t.element_size() for t in houts)
 
     def e2e_step():
-        q.copy_(qh, non_blocking=True)
-        k.copy_(kh, non_blocking=True)
-        v.copy_(vh, non_blocking=True)
-        fa.fwd(q, k, v, causal=prob.causal, scale=prob.scale, cu_seqlens=cu, out=o, lse=lse, stream=stream)
-        oh.copy_(o, non_blocking=True)
-        lh.copy_(lse, non_blocking=True)
+        for dst, src in zip(ins, hins):
+            dst.copy_(src, non_blocking=True)
+        if args.bwd:
+            fa.bwd(q, k, v, o, lse, do, causal=prob.causal, scale=prob.scale, stream=stream,
+                   dq=dq, dk=dk, dv=dv, delta=dl)
+        else:
+            fa.fwd(q, k, v, causal=prob.causal, scale=prob.scale, cu_seqlens=cu, out=o, lse=lse, stream=stream)
+        for dst, src in zip(houts, outs):
+            dst.copy_(src, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -383,7 +427,21 @@ def run_ours(args):
     peaks = load_peaks()
     tag = "of measured" if peaks["source"] == "measured" else "of fallback"
     launch_s = ms_total / args.steps * 1e-3
-    if is_decode(prob):
+    if args.bwd:
+        # The whole backward step (delta, dQ and dK/dV kernels) against the
+        # dense bf16 peak, credited with the plain gradient's FLOPs only.
+        achieved = flops / launch_s / 1e12
+        sustained = ms_total >= 1000.0
+        peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": load_traffic(name + ":bwd", "fa_bwd"),
+                    "peak_kind": "bf16 dense %s %s" % ("sustained" if sustained else "burst", tag),
+                    "frac_of_burst": achieved / peaks["bf16_tflops"],
+                    "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+                    "kernel": "fa_bwd", "algorithmic_flop_per_launch": flops,
+                    "executed_flop_per_launch": prob.flops() * 3.5,
+                    "note": "one step = bwd_delta_kernel + bwd_dq_kernel + bwd_dkdv_kernel"}
+    elif is_decode(prob):
         # Split-KV path: bound by reading K and V from HBM.
         achieved = prob.io_bytes() / launch_s / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -404,7 +462,8 @@ def run_ours(args):
                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                     "kernel": "fa_fwd_kernel", "algorithmic_flop_per_launch": flops,
                     "algorithmic_bytes_per_launch": prob.io_bytes()}
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+    line = {"metric": METRIC_BWD if args.bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(workload_config(prob, name), parallelism="replicas" if world > 1 else "single",
@@ -413,12 +472,12 @@ def run_ours(args):
             "roofline": roofline,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * launches_per_step,
             "clocks": clocks,
             "device_status": status_bits,
             "kernel_sha": kernel_hash(roofline["kernel"])}
     if rank == 0 and not args.no_cpu_baseline:
-        v_cpu, threads, desc, _ = oracle_sample(prob, args.cpu_budget_s)
+        v_cpu, threads, desc, _ = oracle_sample(prob, args.cpu_budget_s, backward=args.bwd)
         line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
     if rank == 0:
         print(json.dumps(line))

@@ -105,13 +105,16 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
 
 def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
         dout: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
-        stream: Optional[torch.cuda.Stream] = None):
+        stream: Optional[torch.cuda.Stream] = None, dq: Optional[torch.Tensor] = None,
+        dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+        delta: Optional[torch.Tensor] = None):
     """Gradients of exact attention on the GPU; returns (dQ, dK, dV, delta).
 
     Dense layout only: q, o, dout [B, Hq, Nq, d], k/v [B, Hkv, Nk, d] bf16,
     lse [B, Hq, Nq] fp32 from ``fwd`` on the same inputs.  delta [B, Hq, Nq]
-    fp32 is rowsum(dout * o).  Runs on ``stream`` (default: the current
-    stream) without synchronising.
+    fp32 is rowsum(dout * o).  Output tensors may be passed in (dq, dk, dv,
+    delta), otherwise they are allocated.  Runs on ``stream`` (default: the
+    current stream) without synchronising.
     """
     dev = q.device
     _check(q, "q", torch.bfloat16, 4, None)
@@ -128,10 +131,17 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
         raise ValueError("lse must be [B, Hq, Nq]")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    dq = torch.empty_like(q)
-    dk = torch.empty_like(k)
-    dv = torch.empty_like(v)
-    delta = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    def out(t, like, name, dtype=torch.bfloat16):
+        if t is None:
+            return torch.empty(like, dtype=dtype, device=dev)
+        _check(t, name, dtype, len(like), dev)
+        if tuple(t.shape) != tuple(like):
+            raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(like)))
+        return t
+    dq = out(dq, q.shape, "dq")
+    dk = out(dk, k.shape, "dk")
+    dv = out(dv, v.shape, "dv")
+    delta = out(delta, (B, Hq, Nq), "delta", torch.float32)
     with torch.cuda.device(dev):
         s = stream if stream is not None else torch.cuda.current_stream(dev)
         st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),

@@ -54,25 +54,63 @@ constexpr int TILE = 128;          // rows per Q, dO, K or V tile (= TMEM lanes)
 constexpr int NUM_THREADS = 320;
 constexpr int WARP_PRODUCER = 8;
 constexpr int WARP_MMA = 9;
-constexpr int SOFTMAX_THREADS = 256;
+constexpr int SOFTMAX_WARPS = 8;
 constexpr float LOG2E = 1.4426950408889634f;
+// Software exponentials: in tiles without a mask, one score pair in every
+// SOFT_EXP_PERIOD is exponentiated on the FMA/ALU pipes (exp2_soft2) instead
+// of the MUFU unit; 0 turns this off.  Off by default: measured on GB300 for
+// B2/H32/N4096/d128 causal, 1 pair in 2 made the backward 11% slower and 1 in
+// 4 3% slower, once the softmax overlaps the tensor pipe (the FMA pipes are
+// busier than the MUFU unit there).
+#ifndef FA_BWD_SOFT_EXP_PERIOD
+#define FA_BWD_SOFT_EXP_PERIOD 0
+#endif
+constexpr int SOFT_EXP_PERIOD = FA_BWD_SOFT_EXP_PERIOD;
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+// p = 2^x for a pair, on the MUFU unit or (soft) on the FMA/ALU pipes.
+// Called from fully unrolled loops, where `soft` is a compile-time constant.
+__device__ __forceinline__ float2 exp2_pair(float2 x, bool soft) {
+  if (soft) return exp2_soft2(x);
+  return make_float2(ex2_approx(x.x), ex2_approx(x.y));
+}
+
+// Whether column pair i goes to the software exponential.
+__device__ __forceinline__ constexpr bool soft_pair(int i) {
+  return SOFT_EXP_PERIOD > 0 && i % (SOFT_EXP_PERIOD > 0 ? SOFT_EXP_PERIOD : 1) == SOFT_EXP_PERIOD - 1;
+}
+
+__device__ __forceinline__ float2 u2f2(uint32_t a, uint32_t b) { return make_float2(__uint_as_float(a), __uint_as_float(b)); }
 
 // Device status word: bit (1 << role) is set when that role gave up waiting.
 // dQ kernel: 0 producer, 1 MMA, 2 softmax; dK/dV kernel: 4, 5, 6.
 __device__ int g_bwd_status;
 
-template <int D>
+// Shared memory of one kernel: two resident tiles (Q and dO for the dQ
+// kernel, K and V for the dK/dV kernel), a ring of NS streamed tiles and, for
+// the dK/dV kernel (KV = true), the LSE and D vectors of two query tiles.
+template <int D, bool KV>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
   static constexpr int TILE_BYTES = TILE * D * 2;
   static constexpr int CHUNKS = D / 64;
   static constexpr int CHUNK_BYTES = TILE * 128;
-  static constexpr int NS = (D == 128) ? 4 : 8;  // ring slots
-  static constexpr int SMEM_FIXED = 2 * TILE_BYTES;  // Q + dO (dQ kernel) or K + V (dK/dV kernel)
+  static constexpr int NS = (D == 128) ? (KV ? 4 : 5) : 8;  // ring slots
+  static constexpr int SMEM_FIXED = 2 * TILE_BYTES;
   static constexpr int SMEM_RING = NS * TILE_BYTES;
-  static constexpr int SMEM_VEC = 2 * 2 * TILE * 4;  // dK/dV kernel: LSE and D of two query tiles
+  static constexpr int SMEM_VEC = KV ? 2 * 2 * TILE * 4 : 0;
   static constexpr int NUM_BARS = 2 * NS + 12;
   static constexpr int SMEM_BYTES = 1024 + SMEM_FIXED + SMEM_RING + SMEM_VEC + NUM_BARS * 8 + 16;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
 struct Params {
@@ -105,11 +143,28 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   return false;
 }
 
+// The same for a whole warp: every lane waits (bounded), and the warp goes on
+// only if all of them saw the phase, so its lanes never split around the
+// warp-collective instructions that follow.
+__device__ __forceinline__ bool warp_wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag, int role,
+                                                   uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, wait_or_abort(bar, parity, abort_flag, role, limit_ns));
+}
+
 // Teardown waits ignore the abort flag: they wait only for copies and
 // products already issued, which complete on their own.
 __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, volatile int* abort_flag, int role,
                                            uint64_t limit_ns, volatile int* never) {
   if (!mbar_wait(bar, parity, never, limit_ns)) raise_abort(abort_flag, role);
+}
+
+// One arrival per softmax warp: every lane has already ordered its own
+// tensor-memory or shared-memory accesses (tcgen05 fence / program order),
+// __syncwarp orders the lanes, and lane 0 arrives with release semantics.
+// (256 single-thread arrivals on one barrier serialise in shared memory.)
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 __device__ __forceinline__ uint32_t elect_leader() {
@@ -157,8 +212,11 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
 // TMEM: [0,128) S   [128,256) dP   [256,256+D) dQ   [384,448) [448,512) dS x2
 // ---------------------------------------------------------------------------
 
-// Unit u -> (batch*head, query tile); heavier (later) query tiles first under
-// a causal mask.
+// Unit u -> (batch*head, query tile); later query tiles (more visible keys
+// under a causal mask) first, so the static schedule deals the heaviest
+// units first.  (Dealing them by groups of heads instead, so that concurrent
+// CTAs share K/V in L2, cut DRAM reads threefold on GB300 but not the time,
+// and slowed the dK/dV kernel by unbalancing the schedule.)
 __device__ __forceinline__ void dq_unit(const Params& p, int u, int& bh, int& qt) {
   const int bh_count = p.B * p.Hq;
   qt = p.nqt - 1 - u / bh_count;
@@ -182,7 +240,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, false>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -199,8 +257,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::NS + s); };
   const uint32_t qfull_bar = bar_base + 8u * (2 * C::NS + 0);
   const uint32_t qempty_bar = bar_base + 8u * (2 * C::NS + 1);
-  const uint32_t sdp_full_bar = bar_base + 8u * (2 * C::NS + 2);
-  const uint32_t sdp_free_bar = bar_base + 8u * (2 * C::NS + 3);
+  // S and dP have their own full (product done) / free (read by every
+  // softmax warp) barriers, so the softmax starts on P while dP is still in
+  // the tensor pipe and the next S is issued as soon as this one is read.
+  const uint32_t s_full_bar = bar_base + 8u * (2 * C::NS + 2);
+  const uint32_t s_free_bar = bar_base + 8u * (2 * C::NS + 3);
+  const uint32_t dp_full_bar = bar_base + 8u * (2 * C::NS + 10);
+  const uint32_t dp_free_bar = bar_base + 8u * (2 * C::NS + 11);
   const uint32_t ds_full_bar = bar_base + 8u * (2 * C::NS + 4);
   auto ds_free_bar = [&](int b) { return bar_base + 8u * (2 * C::NS + 5 + b); };
   const uint32_t dq_done_bar = bar_base + 8u * (2 * C::NS + 7);
@@ -217,13 +280,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(qfull_bar, 1);
     mbar_init(qempty_bar, 1);
-    mbar_init(sdp_full_bar, 1);
-    mbar_init(sdp_free_bar, SOFTMAX_THREADS);
-    mbar_init(ds_full_bar, SOFTMAX_THREADS);
+    mbar_init(s_full_bar, 1);
+    mbar_init(s_free_bar, SOFTMAX_WARPS);
+    mbar_init(dp_full_bar, 1);
+    mbar_init(dp_free_bar, SOFTMAX_WARPS);
+    mbar_init(ds_full_bar, SOFTMAX_WARPS);
     mbar_init(ds_free_bar(0), 1);
     mbar_init(ds_free_bar(1), 1);
     mbar_init(dq_done_bar, 1);
-    mbar_init(dq_free_bar, SOFTMAX_THREADS);
+    mbar_init(dq_free_bar, SOFTMAX_WARPS);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     *never = 0;
@@ -310,13 +375,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!(ok = wait_or_abort(qfull_bar, qcnt & 1u, abort_flag, 1, p.wait_limit_ns))) break;
       ++qcnt;
       const uint32_t it0 = it;
-      // S(g) = Q K_j^T and dP(g) = dO V_j^T for the unit's tile j (global
-      // tile g).  K_j sits in ring fill it0 + 2j, V_j in it0 + 2j + 1.  The
-      // S/dP columns are reused once the softmax warps have read tile g-1.
-      auto sdp = [&](int j) -> bool {
-        const uint32_t g = gt + j;
-        if (g > 0 && !wait_or_abort(sdp_free_bar, (g - 1) & 1u, abort_flag, 1, p.wait_limit_ns)) return false;
-        const uint32_t fk = it0 + 2 * j, fv = fk + 1;
+      // Products of the unit's tile j (global tile g = gt + j); K_j sits in
+      // ring fill it0 + 2j and V_j in it0 + 2j + 1.  Issue order: S(0), dP(0),
+      // then per j: S(j+1), dP(j+1), dQ(j).  S(g) (dP(g)) overwrites the
+      // columns of S(g-1) (dP(g-1)) only after every softmax warp has read
+      // them; the products of this thread complete in issue order.
+      auto issue_s = [&](int j) -> bool {
+        const uint32_t g = gt + j, fk = it0 + 2 * j;
+        if (g > 0 && !wait_or_abort(s_free_bar, (g - 1) & 1u, abort_flag, 1, p.wait_limit_ns)) return false;
         if (!wait_or_abort(full_bar(fk % C::NS), (fk / C::NS) & 1u, abort_flag, 1, p.wait_limit_ns)) return false;
         tc_fence_after();
         const uint64_t k_desc = smem_desc_sw128(ring_addr + (fk % C::NS) * C::TILE_BYTES, 16, 1024);
@@ -325,6 +391,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
           if (leader) umma_ss(tmem + 0, q_desc + off, k_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
         }
+        commit(s_full_bar);
+        return true;
+      };
+      auto issue_dp = [&](int j) -> bool {
+        const uint32_t g = gt + j, fv = it0 + 2 * j + 1;
+        if (g > 0 && !wait_or_abort(dp_free_bar, (g - 1) & 1u, abort_flag, 1, p.wait_limit_ns)) return false;
         if (!wait_or_abort(full_bar(fv % C::NS), (fv / C::NS) & 1u, abort_flag, 1, p.wait_limit_ns)) return false;
         tc_fence_after();
         const uint64_t v_desc = smem_desc_sw128(ring_addr + (fv % C::NS) * C::TILE_BYTES, 16, 1024);
@@ -333,15 +405,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
           if (leader) umma_ss(tmem + 128, do_desc + off, v_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
         }
-        commit(sdp_full_bar);
+        commit(dp_full_bar);
         commit(empty_bar(fv % C::NS));  // V_j is read only by dP
         if (j == nkv - 1) commit(qempty_bar);
         return true;
       };
-      if (!(ok = sdp(0))) break;
+      if (!(ok = issue_s(0) && issue_dp(0))) break;
       for (int j = 0; j < nkv && ok; ++j) {
         const uint32_t g = gt + j;
-        if (j + 1 < nkv && !(ok = sdp(j + 1))) break;
+        if (j + 1 < nkv && !(ok = issue_s(j + 1) && issue_dp(j + 1))) break;
         if (!(ok = wait_or_abort(ds_full_bar, g & 1u, abort_flag, 1, p.wait_limit_ns))) break;
         if (j == 0 && units_done > 0 &&
             !(ok = wait_or_abort(dq_free_bar, (units_done - 1) & 1u, abort_flag, 1, p.wait_limit_ns)))
@@ -398,39 +470,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const float lse2 = row_ok ? __ldg(p.lse + grow) * LOG2E : INFINITY;
       const float dlt = row_ok ? __ldg(p.delta + grow) : 0.f;
       const int lim = row_ok ? (p.causal ? min(p.Nk - 1, row + (p.Nk - p.Nq)) : (p.Nk - 1)) : -1;
+      const float2 c2 = make_float2(sl2, sl2), nl2 = make_float2(-lse2, -lse2), dl2 = make_float2(dlt, dlt);
       for (int j = 0; j < nkv; ++j) {
         const uint32_t g = gt + j;
-        if (!(ok = wait_or_abort(sdp_full_bar, g & 1u, abort_flag, 2, p.wait_limit_ns))) break;
+        // P = 2^(s * scale * log2e - LSE * log2e) from S alone; masked columns
+        // get x = -inf, so P = 0.
+        if (!(ok = warp_wait_or_abort(s_full_bar, g & 1u, abort_flag, 2, p.wait_limit_ns))) break;
         tc_fence_after();
-        uint32_t sr[64], dpr[64];
-        tmem_ld64_wait(tS, sr);
-        tmem_ld64_wait(tDP, dpr);
-        tc_fence_before();
-        mbar_arrive(sdp_free_bar);
-        const int rel = lim - (j * TILE + 64 * h);  // columns c <= rel are visible
-        uint32_t pk[32];
+        float pr[64];
+        {
+          uint32_t sr[64];
+          tmem_ld64_wait(tS, sr);
+          tc_fence_before();
+          warp_arrive(s_free_bar);
+          const int rel = lim - (j * TILE + 64 * h);  // columns c <= rel are visible
+          if (__all_sync(0xffffffffu, rel >= 63)) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float ds2[2];
+            for (int i = 0; i < 32; ++i) {
+              const float2 e = exp2_pair(fma2(u2f2(sr[2 * i], sr[2 * i + 1]), c2, nl2), soft_pair(i));
+              pr[2 * i] = e.x;
+              pr[2 * i + 1] = e.y;
+            }
+          } else {
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = 2 * i + e;
-            const float pr = (c <= rel) ? ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, -lse2)) : 0.f;
-            ds2[e] = pr * (__uint_as_float(dpr[c]) - dlt);
+            for (int i = 0; i < 32; ++i) {
+              float2 x = fma2(u2f2(sr[2 * i], sr[2 * i + 1]), c2, nl2);
+              x.x = (2 * i <= rel) ? x.x : -INFINITY;
+              x.y = (2 * i + 1 <= rel) ? x.y : -INFINITY;
+              const float2 e = exp2_pair(x, false);
+              pr[2 * i] = e.x;
+              pr[2 * i + 1] = e.y;
+            }
           }
-          pk[i] = pack_bf16x2(ds2[0], ds2[1]);
         }
-        if (g >= 2 && !(ok = wait_or_abort(ds_free_bar(g & 1u), ((g >> 1) - 1) & 1u, abort_flag, 2, p.wait_limit_ns)))
+        // dS = P (dP - D), in two halves of 32 columns.
+        if (!(ok = warp_wait_or_abort(dp_full_bar, g & 1u, abort_flag, 2, p.wait_limit_ns))) break;
+        if (g >= 2 &&
+            !(ok = warp_wait_or_abort(ds_free_bar(g & 1u), ((g >> 1) - 1) & 1u, abort_flag, 2, p.wait_limit_ns)))
           break;
         tc_fence_after();
-        tmem_st32(tmem + lane_base + 384 + 64 * (g & 1u) + 32 * h, pk);
+        const uint32_t tDS = tmem + lane_base + 384 + 64 * (g & 1u) + 32 * h;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t dpr[32];
+          tmem_ld32_wait(tDP + 32 * half, dpr);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = 32 * half + 2 * i;
+            const float2 ds = mul2(make_float2(pr[c], pr[c + 1]), sub2(u2f2(dpr[2 * i], dpr[2 * i + 1]), dl2));
+            pk[i] = pack_bf16x2(ds.x, ds.y);
+          }
+          tmem_st16(tDS + 16 * half, pk);
+        }
+        tc_fence_before();
+        warp_arrive(dp_free_bar);
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(ds_full_bar);
+        warp_arrive(ds_full_bar);
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
-      if (!(ok = wait_or_abort(dq_done_bar, units_done & 1u, abort_flag, 2, p.wait_limit_ns))) break;
+      if (!(ok = warp_wait_or_abort(dq_done_bar, units_done & 1u, abort_flag, 2, p.wait_limit_ns))) break;
       tc_fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < D / 2; c0 += 32) {
@@ -447,7 +548,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(dq_free_bar);
+      warp_arrive(dq_free_bar);
       gt += nkv;
       ++units_done;
     }
@@ -470,8 +571,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // over scores it has already read.
 // ---------------------------------------------------------------------------
 
-// Unit u -> (batch*kv head, key tile); under a causal mask the first key
-// tiles are read by the most query tiles, so they come first.
+// Unit u -> (batch*kv head, key tile); the first key tiles (read by the most
+// query tiles under a causal mask) come first.
 __device__ __forceinline__ void kv_unit(const Params& p, int u, int& bkv, int& kt) {
   const int n = p.B * p.Hkv;
   kt = u / n;
@@ -492,14 +593,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, true>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sK = smem;
   uint8_t* sV = smem + C::TILE_BYTES;
   uint8_t* sRing = smem + C::SMEM_FIXED;
-  float* sVec = reinterpret_cast<float*>(sRing + C::SMEM_RING);  // [2][LSE*log2e (128), D (128)]
+  float* sVec = reinterpret_cast<float*>(sRing + C::SMEM_RING);  // [2][-LSE*log2e (128), D (128)]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sRing + C::SMEM_RING + C::SMEM_VEC);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NUM_BARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -510,8 +611,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto empty_bar = [&](int s) { return bar_base + 8u * (C::NS + s); };
   const uint32_t kvfull_bar = bar_base + 8u * (2 * C::NS + 0);
   const uint32_t kvempty_bar = bar_base + 8u * (2 * C::NS + 1);
-  const uint32_t sdp_full_bar = bar_base + 8u * (2 * C::NS + 2);
-  const uint32_t pds_full_bar = bar_base + 8u * (2 * C::NS + 3);
+  // S^T and dP^T products done (commits); P^T and dS^T written back by every
+  // softmax warp (arrivals).
+  const uint32_t s_full_bar = bar_base + 8u * (2 * C::NS + 2);
+  const uint32_t p_full_bar = bar_base + 8u * (2 * C::NS + 3);
+  const uint32_t dp_full_bar = bar_base + 8u * (2 * C::NS + 9);
+  const uint32_t ds_full_bar = bar_base + 8u * (2 * C::NS + 10);
   const uint32_t dkv_done_bar = bar_base + 8u * (2 * C::NS + 4);
   const uint32_t dkv_free_bar = bar_base + 8u * (2 * C::NS + 5);
   const uint32_t drain_bar = bar_base + 8u * (2 * C::NS + 6);
@@ -527,14 +632,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    mbar_init(vec_bar(0), SOFTMAX_THREADS);
-    mbar_init(vec_bar(1), SOFTMAX_THREADS);
+    mbar_init(vec_bar(0), SOFTMAX_WARPS);
+    mbar_init(vec_bar(1), SOFTMAX_WARPS);
     mbar_init(kvfull_bar, 1);
     mbar_init(kvempty_bar, 1);
-    mbar_init(sdp_full_bar, 1);
-    mbar_init(pds_full_bar, SOFTMAX_THREADS);
+    mbar_init(s_full_bar, 1);
+    mbar_init(p_full_bar, SOFTMAX_WARPS);
+    mbar_init(dp_full_bar, 1);
+    mbar_init(ds_full_bar, SOFTMAX_WARPS);
     mbar_init(dkv_done_bar, 1);
-    mbar_init(dkv_free_bar, SOFTMAX_THREADS);
+    mbar_init(dkv_free_bar, SOFTMAX_WARPS);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     *never = 0;
@@ -621,47 +728,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int ntiles = p.group * (p.nqt - i0);
       if (!(ok = wait_or_abort(kvfull_bar, kvcnt & 1u, abort_flag, 5, p.wait_limit_ns))) break;
       ++kvcnt;
-      for (int t = 0; t < ntiles && ok; ++t) {
-        const uint32_t g = gt + t;
-        const uint32_t fq = it, fd = it + 1;
-        const int sq = fq % C::NS, sd = fd % C::NS;
-        if (!(ok = wait_or_abort(full_bar(sq), (fq / C::NS) & 1u, abort_flag, 5, p.wait_limit_ns))) break;
+      // Products of the unit's query tile t (global tile g = gt + t); Q(t)
+      // sits in ring fill it0 + 2t and dO(t) in it0 + 2t + 1.  Issue order:
+      // S^T(0), dP^T(0), then per t: dV(t), S^T(t+1), dK(t), dP^T(t+1).
+      // S^T(t+1) overwrites the P^T that dV(t) reads, and dP^T(t+1) the dS^T
+      // that dK(t) reads, after them in this thread's issue order; the
+      // softmax has read S^T(t) (dP^T(t)) before it signals P (dS) ready.
+      const uint32_t it0 = it;
+      auto issue_s = [&](int t) -> bool {
+        const uint32_t fq = it0 + 2 * t;
+        if (!wait_or_abort(full_bar(fq % C::NS), (fq / C::NS) & 1u, abort_flag, 5, p.wait_limit_ns)) return false;
         tc_fence_after();
-        const uint64_t q_desc = smem_desc_sw128(ring_addr + sq * C::TILE_BYTES, 16, 1024);
+        const uint64_t q_desc = smem_desc_sw128(ring_addr + (fq % C::NS) * C::TILE_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
           if (leader) umma_ss(tmem + 0, k_desc + off, q_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
         }
-        if (!(ok = wait_or_abort(full_bar(sd), (fd / C::NS) & 1u, abort_flag, 5, p.wait_limit_ns))) break;
+        commit(s_full_bar);
+        return true;
+      };
+      auto issue_dp = [&](int t) -> bool {
+        const uint32_t fd = it0 + 2 * t + 1;
+        if (!wait_or_abort(full_bar(fd % C::NS), (fd / C::NS) & 1u, abort_flag, 5, p.wait_limit_ns)) return false;
         tc_fence_after();
-        const uint64_t do_desc = smem_desc_sw128(ring_addr + sd * C::TILE_BYTES, 16, 1024);
+        const uint64_t do_desc = smem_desc_sw128(ring_addr + (fd % C::NS) * C::TILE_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
           if (leader) umma_ss(tmem + 128, v_desc + off, do_desc + off, IDESC_S, kk > 0 ? 1u : 0u);
         }
-        commit(sdp_full_bar);
-        if (!(ok = wait_or_abort(pds_full_bar, g & 1u, abort_flag, 5, p.wait_limit_ns))) break;
-        if (t == 0 && units_done > 0 &&
-            !(ok = wait_or_abort(dkv_free_bar, (units_done - 1) & 1u, abort_flag, 5, p.wait_limit_ns)))
-          break;
+        commit(dp_full_bar);
+        return true;
+      };
+      // dV += P^T dO(t) and dK += dS^T Q(t): A from TMEM (warpgroup w's query
+      // pairs at columns 64 w + 8 (kk % 4)), B MN-major from the ring.
+      auto issue_grad = [&](int t, bool dk) -> bool {
+        const uint32_t g = gt + t, f = it0 + 2 * t + (dk ? 0 : 1);
+        if (!wait_or_abort(dk ? ds_full_bar : p_full_bar, g & 1u, abort_flag, 5, p.wait_limit_ns)) return false;
+        if (!dk && t == 0 && units_done > 0 &&
+            !wait_or_abort(dkv_free_bar, (units_done - 1) & 1u, abort_flag, 5, p.wait_limit_ns))
+          return false;
         tc_fence_after();
-        const uint64_t do_mn = smem_desc_sw128(ring_addr + sd * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
-        const uint64_t q_mn = smem_desc_sw128(ring_addr + sq * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+        const uint64_t b_mn = smem_desc_sw128(ring_addr + (f % C::NS) * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+        const uint32_t d_col = dk ? 384 : 256, a_col = dk ? 128 : 0;
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk) {
-          const uint32_t acol = 64 * (kk / 4) + 8 * (kk % 4);  // query pairs of warpgroup kk/4
-          const uint64_t boff = static_cast<uint64_t>(kk * 16 * 128) >> 4;
-          if (leader) {
-            umma_ts(tmem + 256, tmem + acol, do_mn + boff, IDESC_G, (t > 0 || kk > 0) ? 1u : 0u);
-            umma_ts(tmem + 384, tmem + 128 + acol, q_mn + boff, IDESC_G, (t > 0 || kk > 0) ? 1u : 0u);
-          }
+          const uint32_t acol = a_col + 64 * (kk / 4) + 8 * (kk % 4);
+          if (leader)
+            umma_ts(tmem + d_col, tmem + acol, b_mn + (static_cast<uint64_t>(kk * 16 * 128) >> 4), IDESC_G,
+                    (t > 0 || kk > 0) ? 1u : 0u);
         }
-        commit(empty_bar(sq));
-        commit(empty_bar(sd));
-        it += 2;
+        commit(empty_bar(f % C::NS));  // dO(t) after dV, Q(t) after dK
+        return true;
+      };
+      if (!(ok = issue_s(0) && issue_dp(0))) break;
+      for (int t = 0; t < ntiles && ok; ++t) {
+        const bool more = t + 1 < ntiles;
+        ok = issue_grad(t, false) && (!more || issue_s(t + 1)) && issue_grad(t, true) && (!more || issue_dp(t + 1));
       }
+      it = it0 + 2 * ntiles;
       if (!ok) break;
       commit(dkv_done_bar);
       commit(kvempty_bar);
@@ -708,7 +834,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int qh = kvh * p.group + t / per_head;
         const int q = (i0 + t % per_head) * TILE + (tt & 127);
         const long long qrow = (static_cast<long long>(b) * p.Hq + qh) * p.Nq + q;
-        if (tt < 128) return q < p.Nq ? __ldg(p.lse + qrow) * LOG2E : INFINITY;
+        if (tt < 128) return q < p.Nq ? -__ldg(p.lse + qrow) * LOG2E : -INFINITY;
         return q < p.Nq ? __ldg(p.delta + qrow) : 0.f;
       };
       float v_next = vec_value(0);
@@ -718,10 +844,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // vec_bar of tile g - 1 since, which it reached only after that.
         float* vec = sVec + (g & 1u) * 256;
         vec[tt] = v_next;
-        mbar_arrive(vec_bar(g & 1u));
+        warp_arrive(vec_bar(g & 1u));
         if (t + 1 < ntiles) v_next = vec_value(t + 1);
-        if (!(ok = wait_or_abort(vec_bar(g & 1u), (g >> 1) & 1u, abort_flag, 6, p.wait_limit_ns))) break;
-        if (!(ok = wait_or_abort(sdp_full_bar, g & 1u, abort_flag, 6, p.wait_limit_ns))) break;
+        if (!(ok = warp_wait_or_abort(vec_bar(g & 1u), (g >> 1) & 1u, abort_flag, 6, p.wait_limit_ns))) break;
+        if (!(ok = warp_wait_or_abort(s_full_bar, g & 1u, abort_flag, 6, p.wait_limit_ns))) break;
         tc_fence_after();
         const int q0 = (i0 + t % per_head) * TILE + 64 * h;
         // Query column c is visible to this key iff the query exists
@@ -729,37 +855,74 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // the query's diagonal (c >= cmin).
         const int qmax = p.Nq - 1 - q0;
         const int cmin = p.causal ? key - shift - q0 : -0x40000000;
-        // Two halves of 32 columns; each half's P^T / dS^T (16 packed
-        // columns) lands over scores already read.
+        const float4* nlse4 = reinterpret_cast<const float4*>(vec + 64 * h);
+        const float4* dlt4 = reinterpret_cast<const float4*>(vec + 128 + 64 * h);
+        const float2 c2 = make_float2(sl2, sl2);
+        const bool all_vis = __all_sync(0xffffffffu, key_ok && qmax >= 63 && cmin <= 0);
+        // P^T = 2^(s * scale * log2e - LSE * log2e), masked columns 0; each
+        // half of 32 columns lands (bf16 pairs) over scores already read.
+        float pr[64];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          uint32_t sr[32], dpr[32];
+          uint32_t sr[32];
           tmem_ld32_wait(tS + 32 * half, sr);
-          tmem_ld32_wait(tDP + 32 * half, dpr);
-          uint32_t ppk[16], dpk[16];
+          uint32_t ppk[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float pr[2], ds[2];
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 l4 = nlse4[8 * half + i4];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int c = 32 * half + 2 * i + e;
-              const bool vis = key_ok && c <= qmax && c >= cmin;
-              pr[e] = vis ? ex2_approx(fmaf(__uint_as_float(sr[2 * i + e]), sl2, -vec[64 * h + c])) : 0.f;
-              ds[e] = pr[e] * (__uint_as_float(dpr[2 * i + e]) - vec[128 + 64 * h + c]);
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const int i = 2 * i4 + e2;  // pair i of this half: columns c, c + 1
+              const int c = 32 * half + 2 * i;
+              float2 x = fma2(u2f2(sr[2 * i], sr[2 * i + 1]), c2, e2 ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
+              float2 e;
+              if (all_vis) {
+                e = exp2_pair(x, soft_pair(i));
+              } else {
+                x.x = (key_ok && c <= qmax && c >= cmin) ? x.x : -INFINITY;
+                x.y = (key_ok && c + 1 <= qmax && c + 1 >= cmin) ? x.y : -INFINITY;
+                e = exp2_pair(x, false);
+              }
+              pr[c] = e.x;
+              pr[c + 1] = e.y;
+              ppk[i] = pack_bf16x2(e.x, e.y);
             }
-            ppk[i] = pack_bf16x2(pr[0], pr[1]);
-            dpk[i] = pack_bf16x2(ds[0], ds[1]);
           }
           tmem_st16(tS + 16 * half, ppk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(p_full_bar);
+        // dS^T = P^T (dP^T - D), likewise over dP^T.
+        if (!(ok = warp_wait_or_abort(dp_full_bar, g & 1u, abort_flag, 6, p.wait_limit_ns))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t dpr[32];
+          tmem_ld32_wait(tDP + 32 * half, dpr);
+          uint32_t dpk[16];
+#pragma unroll
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const float4 d4 = dlt4[8 * half + i4];
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const int i = 2 * i4 + e2;
+              const int c = 32 * half + 2 * i;
+              const float2 ds = mul2(make_float2(pr[c], pr[c + 1]),
+                                     sub2(u2f2(dpr[2 * i], dpr[2 * i + 1]),
+                                          e2 ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y)));
+              dpk[i] = pack_bf16x2(ds.x, ds.y);
+            }
+          }
           tmem_st16(tDP + 16 * half, dpk);
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive(pds_full_bar);
+        warp_arrive(ds_full_bar);
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
-      if (!(ok = wait_or_abort(dkv_done_bar, units_done & 1u, abort_flag, 6, p.wait_limit_ns))) break;
+      if (!(ok = warp_wait_or_abort(dkv_done_bar, units_done & 1u, abort_flag, 6, p.wait_limit_ns))) break;
       tc_fence_after();
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
@@ -783,7 +946,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(dkv_free_bar);
+      warp_arrive(dkv_free_bar);
       gt += ntiles;
       ++units_done;
     }
@@ -814,9 +977,9 @@ int bwd_status_and_clear() {
   return v;
 }
 
-int bwd_smem_bytes(int d) {
-  if (d == 64) return bwd::Cfg<64>::SMEM_BYTES;
-  if (d == 128) return bwd::Cfg<128>::SMEM_BYTES;
+int bwd_smem_bytes(int d) {  // the larger of the two main kernels
+  if (d == 64) return max(bwd::Cfg<64, false>::SMEM_BYTES, bwd::Cfg<64, true>::SMEM_BYTES);
+  if (d == 128) return max(bwd::Cfg<128, false>::SMEM_BYTES, bwd::Cfg<128, true>::SMEM_BYTES);
   return 0;
 }
 
@@ -825,15 +988,16 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
                               const float* lse, void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv,
                               int Nq, int Nk, float scale, int causal, cudaStream_t stream, int sms,
                               unsigned long long wait_limit_ns) {
-  using C = bwd::Cfg<D>;
+  using CQ = bwd::Cfg<D, false>;
+  using CKV = bwd::Cfg<D, true>;
   static bool attr_set[kMaxDevicesDecode] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev >= 0 && dev < kMaxDevicesDecode && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(bwd::bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+    if (cudaFuncSetAttribute(bwd::bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CQ::SMEM_BYTES) !=
             cudaSuccess ||
         cudaFuncSetAttribute(bwd::bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             C::SMEM_BYTES) != cudaSuccess)
+                             CKV::SMEM_BYTES) != cudaSuccess)
       return FA_ERR_CUDA;
     attr_set[dev] = true;
   }
@@ -884,8 +1048,8 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
     prm.num_units = static_cast<int>(units);
     const long long grid = units < sms ? units : sms;
     if (grid > 0) {
-      bwd::bwd_dq_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, C::SMEM_BYTES, stream>>>(tq, tdo, tk,
-                                                                                                       tv, prm);
+      bwd::bwd_dq_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, CQ::SMEM_BYTES, stream>>>(tq, tdo, tk,
+                                                                                                        tv, prm);
       if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
   }
@@ -896,7 +1060,7 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
     prm.num_units = static_cast<int>(units);
     const long long grid = units < sms ? units : sms;
     if (grid > 0) {
-      bwd::bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, C::SMEM_BYTES, stream>>>(
+      bwd::bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, CKV::SMEM_BYTES, stream>>>(
           tq, tdo, tk, tv, prm);
       if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
