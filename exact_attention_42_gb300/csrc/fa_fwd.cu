@@ -43,7 +43,6 @@
 #include <cstdint>
 #include <cstring>
 #include <cmath>
-#include <atomic>
 #include <mutex>
 
 #include "fa.h"
@@ -75,7 +74,6 @@ static_assert(2 * REG_SOFTMAX + REG_OTHER <= 512, "register split exceeds a sub-
 // so unnormalised probabilities stay below 2^TAU.  O / l is unchanged by the
 // choice because P and l always share the same stale max.
 constexpr float TAU = 8.0f;
-constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // default limit per wait: 2 s
 // L2 prefetch of the next unit: issued when the producer starts loading the
 // K/V tile PREFETCH_LEAD tiles before the end of the current unit, covering
 // the next unit's Q tiles and its first PREFETCH_KV_TILES K/V tiles.
@@ -707,59 +705,22 @@ static bool encode_rows_map(CUtensorMap* map, const void* base, int d, long long
   return encode_bf16_rows_map(map, base, d, rows, heads, BLOCK_M);
 }
 
-struct DeviceInfo {
-  bool ok = false;
-  bool supported = false;
-  int sms = 0;
-  bool attr_set[2] = {false, false};
-};
-
-// Test hook state (process-wide): see fa_debug_fault_injection.
-static std::atomic<int> g_fault_mode{0};
-static std::atomic<unsigned long long> g_wait_limit_ns{WAIT_LIMIT_NS};
-
-static constexpr int kMaxDevices = 64;
-static DeviceInfo g_dev[kMaxDevices];
-static std::mutex g_dev_mutex;
-
-static fa_status device_info(int dev, DeviceInfo** out) {
-  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_dev_mutex);
-  DeviceInfo& di = g_dev[dev];
-  if (!di.ok) {
-    int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return FA_ERR_CUDA;
-    di.supported = (major == 10 && minor == 3);
-    di.sms = sms;
-    di.ok = true;
-  }
-  if (!di.supported) return FA_ERR_UNSUPPORTED;
-  *out = &di;
-  return FA_OK;
-}
-
 template <int D>
 static fa_status launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-                        int Nq, int Nk, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  DeviceInfo* di = nullptr;
-  fa_status st = device_info(dev, &di);
-  if (st != FA_OK) return st;
+                        int Nq, int Nk, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream,
+                        const LaunchEnv& env) {
   if (decode_supported(B, Hq, Hkv, Nq, Nk, D, cu_seqlens))
-    return launch_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, stream, di->sms,
-                         g_wait_limit_ns.load());
+    return launch_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, stream, env.sms, env.wait_limit_ns);
   {
-    std::lock_guard<std::mutex> lock(g_dev_mutex);
-    const int idx = (D == 128) ? 1 : 0;
-    if (!di->attr_set[idx]) {
+    static std::mutex mu;
+    static bool attr_set[kMaxDevicesDecode] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (env.device < 0 || env.device >= kMaxDevicesDecode) return FA_ERR_CUDA;
+    if (!attr_set[env.device]) {
       if (cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES) !=
           cudaSuccess)
         return FA_ERR_CUDA;
-      di->attr_set[idx] = true;
+      attr_set[env.device] = true;
     }
   }
   const bool packed = cu_seqlens != nullptr;
@@ -788,21 +749,21 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
   prm.group = Hq / Hkv;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.causal = causal ? 1 : 0;
-  prm.wait_limit_ns = g_wait_limit_ns.load();
-  prm.fault_inject = g_fault_mode.load();
+  prm.wait_limit_ns = env.wait_limit_ns;
+  prm.fault_inject = env.fault_mode;
   long long grid;
   if (packed) {
     prm.nqb = 0;
     prm.num_units = -1;
     // Upper bound on units: every sequence adds at most one partial block.
     const long long bound = static_cast<long long>(Hq) * ((Nq + UNIT_ROWS - 1) / UNIT_ROWS + B);
-    grid = bound < di->sms ? bound : di->sms;
+    grid = bound < env.sms ? bound : env.sms;
   } else {
     prm.nqb = (Nq + UNIT_ROWS - 1) / UNIT_ROWS;
     const long long units = static_cast<long long>(B) * Hq * prm.nqb;
     if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
     prm.num_units = static_cast<int>(units);
-    grid = units < di->sms ? units : di->sms;
+    grid = units < env.sms ? units : env.sms;
   }
   if (grid <= 0) return FA_OK;
   fa_fwd_kernel<D><<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
@@ -810,137 +771,33 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
   return FA_OK;
 }
 
-}  // namespace fa
-
-extern "C" {
-
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
-                 int Nk, int d, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream) {
-  if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
-  if (Hq % Hkv != 0) return FA_ERR_SHAPE;
-  if (cu_seqlens != nullptr && Nq != Nk) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_VALUE;
-  if (B == 0 || Hq == 0 || Nq == 0) return FA_OK;
-  if (q == nullptr || o == nullptr || lse == nullptr) return FA_ERR_NULL;
-  if (Nk > 0 && (k == nullptr || v == nullptr)) return FA_ERR_NULL;
-  auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
-  if (mis16(q) || mis16(o) || (Nk > 0 && (mis16(k) || mis16(v)))) return FA_ERR_ALIGN;
-  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
-  if (cu_seqlens != nullptr && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return FA_ERR_ALIGN;
-  // Row and element offsets are 64-bit; the tensor-map row count must fit 32 bits.
-  if (cu_seqlens == nullptr && static_cast<long long>(B) * Hq > 0x7fffffffLL) return FA_ERR_SHAPE;
-  if (d == 128) return fa::launch<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens, stream);
-  return fa::launch<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens, stream);
+fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int d, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream,
+                     const LaunchEnv& env) {
+  if (d == 128) return launch<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens, stream, env);
+  return launch<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens, stream, env);
 }
 
-const char* fa_status_string(fa_status s) {
-  switch (s) {
-    case FA_OK: return "FA_OK";
-    case FA_ERR_NULL: return "FA_ERR_NULL: a required pointer is NULL";
-    case FA_ERR_SHAPE: return "FA_ERR_SHAPE: invalid sizes";
-    case FA_ERR_ALIGN: return "FA_ERR_ALIGN: misaligned pointer";
-    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim or device not supported";
-    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA call failed";
-    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel wait timed out";
-    case FA_ERR_VALUE: return "FA_ERR_VALUE: scale must be finite and positive";
-  }
-  return "unknown fa_status";
-}
-
-fa_status fa_device_status(int* bits) {
-  if (bits == nullptr) return FA_ERR_NULL;
+int fwd_status_and_clear() {
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, fa::g_fa_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_fa_status, sizeof(int)) != cudaSuccess) return -1;
   const int zero = 0;
-  if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
-  const int dv = fa::decode_status_and_clear();
-  if (dv < 0) return FA_ERR_CUDA;
-  if (dv) v |= 1 << 8;  // the split-KV kernel gave up on a wait
-  const int bv = fa::bwd_status_and_clear();
-  if (bv < 0) return FA_ERR_CUDA;
-  v |= bv << 9;  // backward kernels: roles 0-2 (dQ) and 4-6 (dK/dV)
-  *bits = v;
-  return v ? FA_ERR_TIMEOUT : FA_OK;
+  if (cudaMemcpyToSymbol(g_fa_status, &zero, sizeof(int)) != cudaSuccess) return -1;
+  return v;
 }
 
-fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq,
-                    int Nk, int d, float scale, int causal, cudaStream_t stream) {
-  if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
-  if (Hq % Hkv != 0) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_VALUE;
-  if (B == 0 || Hq == 0 || Nq == 0) return FA_OK;
-  if (!fa::decode_supported(B, Hq, Hkv, Nq, Nk, d, nullptr)) return FA_ERR_UNSUPPORTED;
-  if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr) return FA_ERR_NULL;
-  auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
-  if (mis16(q) || mis16(k) || mis16(v) || mis16(o) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return FA_ERR_ALIGN;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  fa::DeviceInfo* di = nullptr;
-  const fa_status st = fa::device_info(dev, &di);
-  if (st != FA_OK) return st;
-  return fa::launch_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream, di->sms,
-                           fa::g_wait_limit_ns.load());
-}
-
-int fa_decode_smem_bytes(int d) { return fa::decode_smem_bytes(d); }
-
-int fa_bwd_smem_bytes(int d) { return fa::bwd_smem_bytes(d); }
-
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                 void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int Nq, int Nk, int d,
-                 float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream) {
-  if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
-  if (Hq % Hkv != 0) return FA_ERR_SHAPE;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (cu_seqlens != nullptr) return FA_ERR_UNSUPPORTED;
-  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_VALUE;
-  if (B == 0 || Hq == 0 || Nq == 0) return FA_OK;
-  if (q == nullptr || o == nullptr || dout == nullptr || lse == nullptr || dq == nullptr || delta == nullptr)
-    return FA_ERR_NULL;
-  if (Nk > 0 && (k == nullptr || v == nullptr || dk == nullptr || dv == nullptr)) return FA_ERR_NULL;
-  auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
-  if (mis16(q) || mis16(o) || mis16(dout) || mis16(dq)) return FA_ERR_ALIGN;
-  if (Nk > 0 && (mis16(k) || mis16(v) || mis16(dk) || mis16(dv))) return FA_ERR_ALIGN;
-  if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || (reinterpret_cast<uintptr_t>(delta) & 3u) != 0)
-    return FA_ERR_ALIGN;
-  if (static_cast<long long>(B) * Hq > 0x7fffffffLL) return FA_ERR_SHAPE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  fa::DeviceInfo* di = nullptr;
-  const fa_status st = fa::device_info(dev, &di);
-  if (st != FA_OK) return st;
-  return fa::launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream,
-                        di->sms, fa::g_wait_limit_ns.load());
-}
-
-fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds) {
-  if (mode < 0 || mode > 1) return FA_ERR_VALUE;
-  if (!(wait_limit_seconds <= 10.0)) return FA_ERR_VALUE;  // also rejects NaN
-  const unsigned long long ns = wait_limit_seconds > 0.0
-                                    ? static_cast<unsigned long long>(wait_limit_seconds * 1e9)
-                                    : fa::WAIT_LIMIT_NS;
-  fa::g_wait_limit_ns.store(ns);
-  fa::g_fault_mode.store(mode);
-  return FA_OK;
-}
-
-fa_status fa_debug_exp2_soft(const float* x, float* y, int n, cudaStream_t stream) {
-  if (n < 0) return FA_ERR_SHAPE;
-  if (n == 0) return FA_OK;
-  if (x == nullptr || y == nullptr) return FA_ERR_NULL;
+fa_status launch_exp2_soft(const float* x, float* y, int n, cudaStream_t stream) {
   const int pairs = (n + 1) / 2;
-  fa::exp2_soft_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(x, y, n);
+  exp2_soft_kernel<<<(pairs + 255) / 256, 256, 0, stream>>>(x, y, n);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
-int fa_fwd_smem_bytes(int d) {
-  if (d == 64) return fa::Cfg<64>::SMEM_BYTES;
-  if (d == 128) return fa::Cfg<128>::SMEM_BYTES;
+int fwd_smem_bytes(int d) {
+  if (d == 64) return Cfg<64>::SMEM_BYTES;
+  if (d == 128) return Cfg<128>::SMEM_BYTES;
   return 0;
 }
 
-int fa_fwd_threads(void) { return fa::NUM_THREADS; }
+int fwd_threads() { return NUM_THREADS; }
 
-}  // extern "C"
+}  // namespace fa

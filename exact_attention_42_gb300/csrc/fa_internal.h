@@ -9,7 +9,25 @@
 
 namespace fa {
 
-constexpr int kMaxDevicesDecode = 64;
+constexpr int kMaxDevicesDecode = 64;                      // devices with per-device launch state
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // bound on every kernel wait: 2 s
+
+// Per-call launch settings resolved by the entry points (fa_api.cu).
+struct LaunchEnv {
+  int device = 0;
+  int sms = 0;                          // streaming multiprocessors of the device
+  unsigned long long wait_limit_ns = 0;  // bound on every mbarrier wait
+  int fault_mode = 0;                   // test hook, see fa_debug_fault_injection
+};
+
+// Forward kernel (fa_fwd.cu); dispatches to the split-KV path itself.
+fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int d, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream,
+                     const LaunchEnv& env);
+int fwd_status_and_clear();  // -1 if the status word cannot be read
+fa_status launch_exp2_soft(const float* x, float* y, int n, cudaStream_t stream);
+int fwd_smem_bytes(int d);
+int fwd_threads();
 
 // Tensor map of a [heads, rows, d] bf16 tensor read in boxes of 64 columns x
 // box_rows rows with the 128-byte swizzle; false if the driver rejects it.
