@@ -10,7 +10,7 @@ from typing import Optional, Tuple
 
 import torch
 
-from ._lib import FaError, fa_bwd, fa_fwd
+from ._lib import FaError, fa_bwd, fa_fwd, fa_fwd_fp8
 
 
 def _check(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int, device) -> None:
@@ -150,3 +150,44 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
     if st != 0:
         raise FaError(st, "fa_bwd")
     return dq, dk, dv, delta
+
+
+def fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, vt8: torch.Tensor, q_descale: torch.Tensor,
+            k_descale: torch.Tensor, v_descale: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
+            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Attention forward with e4m3 inputs on the GPU; returns (O bf16, LSE fp32).
+
+    q8 [B, Hq, Nq, 128], k8 [B, Hkv, Nk, 128] and vt8 [B, Hkv, 128, Nk] hold
+    e4m3 codes (torch.uint8 or torch.float8_e4m3fn); the descales are fp32
+    [B, Hq], [B, Hkv], [B, Hkv].  Nk must be a multiple of 16.
+    """
+    dev = q8.device
+    as_u8 = lambda t: t.view(torch.uint8) if t.dtype != torch.uint8 else t
+    q8, k8, vt8 = as_u8(q8), as_u8(k8), as_u8(vt8)
+    _check(q8, "q8", torch.uint8, 4, None)
+    _check(k8, "k8", torch.uint8, 4, dev)
+    _check(vt8, "vt8", torch.uint8, 4, dev)
+    B, Hq, Nq, d = q8.shape
+    Bk, Hkv, Nk, dk = k8.shape
+    if Bk != B or dk != d or tuple(vt8.shape) != (B, Hkv, d, Nk):
+        raise ValueError("k8 must be [B, Hkv, Nk, d] and vt8 [B, Hkv, d, Nk]")
+    for t, n, shp in ((q_descale, "q_descale", (B, Hq)), (k_descale, "k_descale", (B, Hkv)),
+                      (v_descale, "v_descale", (B, Hkv))):
+        _check(t, n, torch.float32, 2, dev)
+        if tuple(t.shape) != shp:
+            raise ValueError("%s must be %s" % (n, shp))
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Hq, Nq, d), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        st = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), q_descale.data_ptr(), k_descale.data_ptr(),
+                        v_descale.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Nq, Nk, d, float(scale),
+                        int(bool(causal)), s.cuda_stream)
+    if st != 0:
+        raise FaError(st, "fa_fwd_fp8")
+    return out, lse

@@ -126,6 +126,29 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
 
 int fa_decode_smem_bytes(int d) { return fa::decode_smem_bytes(d); }
 
+fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
+                     const float* k_descale, const float* v_descale, void* o, float* lse, int B, int Hq, int Hkv,
+                     int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream) {
+  if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
+  if (Hq % Hkv != 0) return FA_ERR_SHAPE;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (Nk % 16 != 0) return FA_ERR_SHAPE;  // rows of V^T are Nk bytes: a multiple of 16
+  if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_VALUE;
+  if (B == 0 || Hq == 0 || Nq == 0) return FA_OK;
+  if (q8 == nullptr || q_descale == nullptr || o == nullptr || lse == nullptr) return FA_ERR_NULL;
+  if (Nk > 0 && (k8 == nullptr || vt8 == nullptr || k_descale == nullptr || v_descale == nullptr))
+    return FA_ERR_NULL;
+  auto mis = [](const void* ptr, unsigned a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0; };
+  if (mis(q8, 16) || mis(o, 16) || (Nk > 0 && (mis(k8, 16) || mis(vt8, 16)))) return FA_ERR_ALIGN;
+  if (mis(lse, 4) || mis(q_descale, 4) || (Nk > 0 && (mis(k_descale, 4) || mis(v_descale, 4)))) return FA_ERR_ALIGN;
+  if (static_cast<long long>(B) * Hq > 0x7fffffffLL) return FA_ERR_SHAPE;
+  fa::LaunchEnv env;
+  const fa_status st = fa::launch_env(&env);
+  if (st != FA_OK) return st;
+  return fa::launch_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal,
+                            stream, env);
+}
+
 int fa_bwd_smem_bytes(int d) { return fa::bwd_smem_bytes(d); }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,

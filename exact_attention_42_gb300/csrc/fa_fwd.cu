@@ -74,6 +74,13 @@ static_assert(2 * REG_SOFTMAX + REG_OTHER <= 512, "register split exceeds a sub-
 // so unnormalised probabilities stay below 2^TAU.  O / l is unchanged by the
 // choice because P and l always share the same stale max.
 constexpr float TAU = 8.0f;
+// 8-bit path: P is stored as e4m3 (largest finite 448, smallest subnormal
+// 2^-9).  There the reference max moves whenever a row max grows (threshold
+// 0) and p is taken as 2^(s - m + P_SHIFT_FP8), so 0 < p <= 256 and only
+// terms below 2^-17 of the row max are lost to underflow; l carries the same
+// factor, which O / l cancels and the LSE subtracts.
+constexpr float TAU_FP8 = 0.0f;
+constexpr float P_SHIFT_FP8 = 8.0f;
 // L2 prefetch of the next unit: issued when the producer starts loading the
 // K/V tile PREFETCH_LEAD tiles before the end of the current unit, covering
 // the next unit's Q tiles and its first PREFETCH_KV_TILES K/V tiles.
@@ -93,13 +100,19 @@ constexpr int SOFT_EXP_PERIOD = FA_SOFT_EXP_PERIOD;
 // Device status word: bit (1 << role) is set when that role gave up waiting.
 __device__ int g_fa_status;
 
-template <int D>
+// FP8 selects the 8-bit path: e4m3 Q, K and V^T, products of kind f8f6f4.
+template <int D, bool FP8 = false>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int TILE_BYTES = BLOCK_M * D * 2;   // one 128 x D bf16 tile
-  static constexpr int CHUNKS = D / 64;                // 128-byte swizzle column blocks
+  static_assert(!FP8 || D == 128, "the 8-bit path is built for d = 128");
+  static constexpr int ELEM = FP8 ? 1 : 2;             // bytes per element
+  static constexpr int TILE_BYTES = BLOCK_M * D * ELEM;  // one 128 x D tile
+  static constexpr int CHUNKS = D * ELEM / 128;        // 128-byte swizzle column blocks
+  static constexpr int CHUNK_COLS = 128 / ELEM;        // elements per column block
   static constexpr int CHUNK_BYTES = BLOCK_M * 128;    // 16 KB
-  static constexpr int NS = (D == 128) ? 5 : 8;        // K/V ring slots
+  static constexpr int NS = (TILE_BYTES == 32768) ? 5 : 8;  // K/V ring slots
+  static constexpr int QK_KSTEPS = D * ELEM / 32;      // 32 bytes of K per product
+  static constexpr int PV_KSTEPS = BLOCK_N * ELEM / 32;
   static constexpr int SMEM_Q = NQT * TILE_BYTES;
   static constexpr int SMEM_RING = NS * TILE_BYTES;
   // barriers: full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], drain
@@ -118,6 +131,11 @@ struct Params {
   int num_units;          // dense: B * Hq * nqb; packed: computed on the device
   unsigned long long wait_limit_ns;  // bound on every mbarrier wait
   int fault_inject;       // test hook: 1 = the K/V producer withholds its first fill
+  // 8-bit path only: per-(batch, head) descale factors of Q [B*Hq], K and V
+  // [B*Hkv]; the real inputs are code * descale.
+  const float* q_descale;
+  const float* k_descale;
+  const float* v_descale;
 };
 
 struct Unit {
@@ -201,6 +219,51 @@ __device__ __forceinline__ int kv_tiles(const Params& p, const Unit& w, int t) {
   return last_key / BLOCK_N + 1;
 }
 
+// Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0),
+// fp32 accumulation, both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A * B for 8-bit operands (A in shared or tensor memory).
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four fp32 values to e4m3 (round to nearest even, saturating), x0 in the
+// lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return r;
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+               "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int role) {
   *abort_flag = 1;
   atomicOr(&g_fa_status, 1 << role);
@@ -222,11 +285,11 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, volati
   if (!mbar_wait(bar, parity, &never, limit_ns)) raise_abort(abort_flag, role);
 }
 
-template <int D>
+template <int D, bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, FP8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -308,13 +371,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int t = 0; t < NQT; ++t) {
           if ((t == 0 ? nk0 : nk1) == 0) continue;
           for (int c = 0; c < C::CHUNKS; ++c)
-            tma_prefetch_l2_3d(&tm_q, c * 64, wn.q_y + wn.row0 + t * BLOCK_M, wn.q_z);
+            tma_prefetch_l2_3d(&tm_q, c * C::CHUNK_COLS, wn.q_y + wn.row0 + t * BLOCK_M, wn.q_z);
         }
         const int nn = min(max(nk0, nk1), PREFETCH_KV_TILES);
         for (int j = 0; j < nn; ++j)
           for (int c = 0; c < C::CHUNKS; ++c) {
-            tma_prefetch_l2_3d(&tm_k, c * 64, wn.k_y + j * BLOCK_N, wn.k_z);
-            tma_prefetch_l2_3d(&tm_v, c * 64, wn.k_y + j * BLOCK_N, wn.k_z);
+            tma_prefetch_l2_3d(&tm_k, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
+            if constexpr (FP8)  // V^T: keys along x, head dims along y
+              tma_prefetch_l2_3d(&tm_v, wn.k_y + j * BLOCK_N, 0, wn.k_z);
+            else
+              tma_prefetch_l2_3d(&tm_v, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
           }
       };
       for (int k = 0; k * static_cast<int>(gridDim.x) < num_units && ok; ++k) {
@@ -335,9 +401,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
             const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
-            for (int c = 0; c < C::CHUNKS; ++c)
-              tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, full_bar(s), c * 64, w.k_y + j * BLOCK_N,
-                          w.k_z);
+            if (FP8 && kv) {  // V^T tile: 128 head dims (rows) x 128 keys (bytes)
+              tma_load_3d(dst, &tm_v, full_bar(s), w.k_y + j * BLOCK_N, 0, w.k_z);
+            } else {
+              for (int c = 0; c < C::CHUNKS; ++c)
+                tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, full_bar(s), c * C::CHUNK_COLS,
+                            w.k_y + j * BLOCK_N, w.k_z);
+            }
             ++it;
           }
         }
@@ -367,8 +437,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_arrive_expect_tx(qfull_bar(t), C::TILE_BYTES);
           const uint32_t dst = smem_u32(sQ + t * C::TILE_BYTES);
           for (int c = 0; c < C::CHUNKS; ++c)
-            tma_load_3d(dst + c * C::CHUNK_BYTES, &tm_q, qfull_bar(t), c * 64, w.q_y + w.row0 + t * BLOCK_M,
-                        w.q_z);
+            tma_load_3d(dst + c * C::CHUNK_BYTES, &tm_q, qfull_bar(t), c * C::CHUNK_COLS,
+                        w.q_y + w.row0 + t * BLOCK_M, w.q_z);
           ++qfills[t];
         }
       }
@@ -384,8 +454,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t elected;
     asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(elected));
     const bool leader = elected != 0;
-    constexpr uint32_t IDESC_QK = idesc_bf16_f32(BLOCK_M, BLOCK_N, 0, 0);
-    constexpr uint32_t IDESC_PV = idesc_bf16_f32(BLOCK_M, D, 0, 1);
+    // 8-bit path: both products K-major (V arrives transposed), 32 bytes of K each.
+    constexpr uint32_t IDESC_QK = FP8 ? idesc_e4m3_f32(BLOCK_M, BLOCK_N) : idesc_bf16_f32(BLOCK_M, BLOCK_N, 0, 0);
+    constexpr uint32_t IDESC_PV = FP8 ? idesc_e4m3_f32(BLOCK_M, D) : idesc_bf16_f32(BLOCK_M, D, 0, 1);
     const uint32_t q_addr = smem_u32(sQ);
     const uint32_t ring_addr = smem_u32(sRing);
     // S_t = Q_t K^T: both operands K-major (head dim contiguous), 16 columns per MMA.
@@ -393,19 +464,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t q_desc = smem_desc_sw128(q_addr + t * C::TILE_BYTES, 16, 1024);
       const uint64_t k_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 0; kk < C::QK_KSTEPS; ++kk) {
         const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
-        if (leader) umma_ss(tmem + t * 128, q_desc + off, k_desc + off, IDESC_QK, kk > 0 ? 1u : 0u);
+        if (leader) {
+          if constexpr (FP8)
+            umma_ss_f8(tmem + t * 128, q_desc + off, k_desc + off, IDESC_QK, kk > 0 ? 1u : 0u);
+          else
+            umma_ss(tmem + t * 128, q_desc + off, k_desc + off, IDESC_QK, kk > 0 ? 1u : 0u);
+        }
       }
     };
     // O_t (+)= P_t V: P from TMEM (bf16 pairs), V MN-major (head dim contiguous), 16 keys per MMA.
     auto issue_pv = [&](int t, int slot, bool accumulate) {
-      const uint64_t v_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+      if constexpr (FP8) {
+        // V^T K-major (keys contiguous); P as packed e4m3 in TMEM, 8 columns per 32 keys.
+        const uint64_t vt_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
-        if (leader)
-          umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                  v_desc + static_cast<uint64_t>(kk * 16 * 128 >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
+          if (leader)
+            umma_ts_f8(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, vt_desc + static_cast<uint64_t>(kk * 32 >> 4),
+                       IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+        }
+      } else {
+        const uint64_t v_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+#pragma unroll
+        for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
+          if (leader)
+            umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                    v_desc + static_cast<uint64_t>(kk * 16 * 128 >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+        }
       }
     };
     auto commit = [&](uint32_t bar) {
@@ -497,8 +584,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + 256 + t * 128;
-    const float sl2 = p.scale_log2;
+    const float sl2_base = p.scale_log2;
     const float NEG_INF = -INFINITY;
+    constexpr float tau = FP8 ? TAU_FP8 : TAU;
+    constexpr float p_shift = FP8 ? P_SHIFT_FP8 : 0.f;
     uint32_t scnt = 0, ocnt = 0;
     bool ok = true;
     for (int k = 0; k * static_cast<int>(gridDim.x) < num_units && ok; ++k) {
@@ -513,6 +602,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool row_ok = row < w.Lq;
       const int diag = row + (w.Lk - w.Lq);  // last visible key under the causal mask
       const int tile_diag = q0 + (w.Lk - w.Lq);
+      // 8-bit path: the Q and K descales scale every score of this unit.
+      float sl2 = sl2_base;
+      if constexpr (FP8) sl2 *= __ldg(p.q_descale + w.q_z) * __ldg(p.k_descale + w.k_z);
       float m_used = NEG_INF;
       float l = 0.f;
       for (int j = 0; j < nkv; ++j) {
@@ -550,7 +642,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const float mx = max3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
         const float m_tile = mx * sl2;
         const float m_new = fmaxf(m_used, m_tile);
-        const bool need = m_new > m_used + TAU;
+        const bool need = m_new > m_used + tau;
         if (j == 0) {
           m_used = m_new;
         } else if (__any_sync(0xffffffffu, need)) {
@@ -568,7 +660,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           l *= alpha;
           if (need) m_used = m_new;
         }
-        const float neg_base = (m_used == NEG_INF) ? 0.f : -m_used;
+        const float neg_base = (m_used == NEG_INF) ? 0.f : p_shift - m_used;
         // p = 2^(s * scale * log2e - m_used), two scores per packed FMA; the
         // row sum runs in four packed accumulators.
         const float2 c2 = make_float2(sl2, sl2);
@@ -578,11 +670,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c0 = 0; c0 < BLOCK_N; c0 += 32) {
-          uint32_t pk[16];
+          uint32_t pk[16];   // bf16 pairs
+          uint32_t pk8[8];   // 8-bit path: e4m3 quads
           if (c0 > rel_hi) {  // hidden from every lane of the warp: P = 0
 #pragma unroll
             for (int i = 0; i < 16; ++i) pk[i] = 0u;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pk8[i] = 0u;
           } else {
+            float2 prev = make_float2(0.f, 0.f);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const float2 x = fma2(make_float2(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nb2);
@@ -593,10 +689,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               else
                 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
               acc[i % 4] = add2(acc[i % 4], e);
-              pk[i] = pack_bf16x2(e.x, e.y);
+              if constexpr (FP8) {
+                if (i & 1) pk8[i / 2] = pack_e4m3x4(prev.x, prev.y, e.x, e.y);
+                prev = e;
+              } else {
+                pk[i] = pack_bf16x2(e.x, e.y);
+              }
             }
           }
-          tmem_st16(tS + c0 / 2, pk);
+          if constexpr (FP8)
+            tmem_st8(tS + c0 / 4, pk8);
+          else
+            tmem_st16(tS + c0 / 2, pk);
         }
         {
           const float2 a01 = add2(acc[0], acc[1]);
@@ -615,7 +719,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++ocnt;
         tc_fence_after();
       }
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      if constexpr (FP8) inv_l *= __ldg(p.v_descale + w.k_z);
       __nv_bfloat16* orow = p.o + (w.out_row + row) * D;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -637,7 +742,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if (row_ok) {
-        const float lse = (l > 0.f) ? (m_used + __log2f(l)) * 0.69314718055994531f : NEG_INF;
+        const float lse = (l > 0.f) ? (m_used - p_shift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
         p.lse[w.out_row + row] = lse;
       }
     }
@@ -717,8 +822,8 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
     std::lock_guard<std::mutex> lock(mu);
     if (env.device < 0 || env.device >= kMaxDevicesDecode) return FA_ERR_CUDA;
     if (!attr_set[env.device]) {
-      if (cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES) !=
-          cudaSuccess)
+      if (cudaFuncSetAttribute(fa_fwd_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<D>::SMEM_BYTES) != cudaSuccess)
         return FA_ERR_CUDA;
       attr_set[env.device] = true;
     }
@@ -751,6 +856,7 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
   prm.causal = causal ? 1 : 0;
   prm.wait_limit_ns = env.wait_limit_ns;
   prm.fault_inject = env.fault_mode;
+  prm.q_descale = prm.k_descale = prm.v_descale = nullptr;
   long long grid;
   if (packed) {
     prm.nqb = 0;
@@ -766,7 +872,7 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
     grid = units < env.sms ? units : env.sms;
   }
   if (grid <= 0) return FA_OK;
-  fa_fwd_kernel<D><<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+  fa_fwd_kernel<D, false><<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -776,6 +882,72 @@ fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float
                      const LaunchEnv& env) {
   if (d == 128) return launch<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens, stream, env);
   return launch<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens, stream, env);
+}
+
+// [heads, rows, cols] uint8 tensor read in 128-row x 128-byte boxes with the
+// 128-byte swizzle (the K-major layout of an 8-bit operand tile).
+static bool encode_u8_map(CUtensorMap* map, const void* base, long long cols, long long rows, long long heads) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows * cols)};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(BLOCK_M), 1};
+  cuuint32_t elem[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, elem,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
+                         const float* k_descale, const float* v_descale, void* o, float* lse, int B, int Hq, int Hkv,
+                         int Nq, int Nk, float scale, int causal, cudaStream_t stream, const LaunchEnv& env) {
+  constexpr int D = 128;
+  using C = Cfg<D, true>;
+  {
+    static std::mutex mu;
+    static bool attr_set[kMaxDevicesDecode] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (env.device < 0 || env.device >= kMaxDevicesDecode) return FA_ERR_CUDA;
+    if (!attr_set[env.device]) {
+      if (cudaFuncSetAttribute(fa_fwd_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+          cudaSuccess)
+        return FA_ERR_CUDA;
+      attr_set[env.device] = true;
+    }
+  }
+  alignas(64) CUtensorMap tq, tk, tv;
+  std::memset(&tk, 0, sizeof(tk));
+  std::memset(&tv, 0, sizeof(tv));
+  if (!encode_u8_map(&tq, q8, D, Nq, static_cast<long long>(B) * Hq)) return FA_ERR_CUDA;
+  if (Nk > 0 && (!encode_u8_map(&tk, k8, D, Nk, static_cast<long long>(B) * Hkv) ||
+                 !encode_u8_map(&tv, vt8, Nk, D, static_cast<long long>(B) * Hkv)))
+    return FA_ERR_CUDA;
+  Params prm;
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.cu_seqlens = nullptr;
+  prm.B = B;
+  prm.Hq = Hq;
+  prm.Hkv = Hkv;
+  prm.Nq = Nq;
+  prm.Nk = Nk;
+  prm.group = Hq / Hkv;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.causal = causal ? 1 : 0;
+  prm.wait_limit_ns = env.wait_limit_ns;
+  prm.fault_inject = 0;
+  prm.q_descale = q_descale;
+  prm.k_descale = k_descale;
+  prm.v_descale = v_descale;
+  prm.nqb = (Nq + UNIT_ROWS - 1) / UNIT_ROWS;
+  const long long units = static_cast<long long>(B) * Hq * prm.nqb;
+  if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
+  prm.num_units = static_cast<int>(units);
+  const long long grid = units < env.sms ? units : env.sms;
+  if (grid <= 0) return FA_OK;
+  fa_fwd_kernel<D, true><<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+  return FA_OK;
 }
 
 int fwd_status_and_clear() {

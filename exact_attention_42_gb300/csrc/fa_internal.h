@@ -24,6 +24,11 @@ struct LaunchEnv {
 fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                      int Nq, int Nk, int d, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream,
                      const LaunchEnv& env);
+// 8-bit forward (fa_fwd.cu, d = 128, dense): e4m3 Q, K and V^T with
+// per-(batch, head) descales.
+fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
+                         const float* k_descale, const float* v_descale, void* o, float* lse, int B, int Hq, int Hkv,
+                         int Nq, int Nk, float scale, int causal, cudaStream_t stream, const LaunchEnv& env);
 int fwd_status_and_clear();  // -1 if the status word cannot be read
 fa_status launch_exp2_soft(const float* x, float* y, int n, cudaStream_t stream);
 int fwd_smem_bytes(int d);

@@ -127,6 +127,89 @@ def uniform_ints(key: int, count: int, lo: int, hi: int) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------
+# FP8 (e4m3) encoding, for the 8-bit forward path's inputs
+# --------------------------------------------------------------------------
+# OCP 8-bit floating point, E4M3 variant: 1 sign, 4 exponent (bias 7) and 3
+# mantissa bits; no infinities; S.1111.111 is NaN, so the largest finite
+# magnitude is 1.75 * 2^8 = 448; subnormals go down to 2^-9.
+
+E4M3_MAX = 448.0
+
+
+def e4m3_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact value of each e4m3 code (NaN for the two NaN codes)."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    val = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    val = np.where((e == 0xF) & (m == 7), np.nan, val)
+    return sign * val
+
+
+_E4M3_TABLE = e4m3_bits_to_f64(np.arange(128, dtype=np.uint8))  # non-negative codes, increasing
+
+
+def f64_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest e4m3 value (ties to the even code), saturating at
+    +-448; finite inputs."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    finite = _E4M3_TABLE[:127]  # codes 0..126 (127 is NaN)
+    hi = np.clip(np.searchsorted(finite, a, side="left"), 0, 126)
+    lo = np.clip(hi - 1, 0, 126)
+    dlo = a - finite[lo]
+    dhi = finite[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0) & (hi != lo))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    return np.where(x < 0, code | 0x80, code).astype(np.uint8)
+
+
+@dataclasses.dataclass
+class Fp8Problem:
+    """A dense problem quantized to e4m3 with one scale per (batch, head).
+
+    q8 [B, Hq, Nq, d], k8 [B, Hkv, Nk, d] and vt8 [B, Hkv, d, Nk] (V
+    transposed) are e4m3 codes; the real inputs are q8 * q_scale[b, h] and so
+    on.  Each scale is the tensor slice's max |x| / 448 (1 for an all-zero
+    slice), so the slice uses the whole e4m3 range.
+    """
+    base: "Problem"
+    q8: np.ndarray
+    k8: np.ndarray
+    vt8: np.ndarray
+    q_scale: np.ndarray  # [B, Hq] float32
+    k_scale: np.ndarray  # [B, Hkv] float32
+    v_scale: np.ndarray  # [B, Hkv] float32
+
+    def dequantized(self):
+        """(q, k, v) as float64 arrays in the dense layout."""
+        q = e4m3_bits_to_f64(self.q8) * self.q_scale.astype(np.float64)[:, :, None, None]
+        k = e4m3_bits_to_f64(self.k8) * self.k_scale.astype(np.float64)[:, :, None, None]
+        vt = e4m3_bits_to_f64(self.vt8) * self.v_scale.astype(np.float64)[:, :, None, None]
+        return q, k, np.swapaxes(vt, 2, 3)
+
+
+def _quantize_slices(x: np.ndarray):
+    """Per-[b, h] scale (float32) and e4m3 codes of x / scale."""
+    amax = np.max(np.abs(x), axis=(2, 3)) if x.size else np.zeros(x.shape[:2])
+    scale = np.where(amax > 0, amax / E4M3_MAX, 1.0).astype(np.float32)
+    codes = f64_to_e4m3_bits(x / scale.astype(np.float64)[:, :, None, None])
+    return codes, scale
+
+
+def make_fp8(prob: "Problem") -> Fp8Problem:
+    """Quantizes a dense bf16 problem's Q, K, V to e4m3 (V also transposed)."""
+    assert prob.cu_seqlens is None, "the 8-bit path takes dense problems"
+    q, k, v = (bf16_bits_to_f64(x) for x in (prob.q, prob.k, prob.v))
+    q8, qs = _quantize_slices(q)
+    k8, ks = _quantize_slices(k)
+    v8, vs = _quantize_slices(v)
+    vt8 = np.ascontiguousarray(np.swapaxes(v8, 2, 3))
+    return Fp8Problem(prob, q8, k8, vt8, qs, ks, vs)
+
+
+# --------------------------------------------------------------------------
 # Workloads
 # --------------------------------------------------------------------------
 
@@ -229,6 +312,8 @@ WORKLOADS = {
 }
 
 HEADLINE = "b2_h32_n4096_d128_causal"
+# Workloads the 8-bit forward path is measured on (quantized with make_fp8).
+FP8_WORKLOADS = ("b2_h32_n4096_d128_causal", "gqa_b1_hq32_hkv8_n16384_d128_causal")
 
 
 def make_workload(name: str) -> Problem:

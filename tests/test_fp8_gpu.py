@@ -1,0 +1,117 @@
+"""GPU parity of the 8-bit forward (fa_fwd_fp8) against the fp64 oracle.
+
+The oracle runs the plain definition on the dequantized inputs (e4m3 code x
+descale, exactly representable in float64), so the only departure of the
+kernel from it is P rounded to e4m3 before the P V product, plus fp32
+accumulation and the bf16 output.  Rounding changes each term p_j v_j by at
+most 2^-4 of itself, so for every output element
+
+    |O_gpu - O_ref| <= 2^-4 * (sum_j p_j |v_j|) / l + 2^-8 |O_ref| + 2e-3,
+
+where the first term is the oracle's attention with |V| in place of V, the
+second the bf16 rounding of O and the last covers fp32 accumulation and the
+exponential.  LSE is formed from the unrounded p and keeps the fp16-path
+tolerance (1e-3 relative).
+"""
+import numpy as np
+import pytest
+import torch
+
+from fa_inputs import make_dense, make_fp8, make_workload
+from fa_testutil import LSE_RTOL
+from oracle import attention_fwd, attention_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import exact_attention_42_gb300 as m
+    m.build()
+    m.lib()
+    return m
+
+
+@pytest.fixture(scope="module")
+def dev():
+    return torch.device("cuda", 0)
+
+
+@pytest.fixture(autouse=True)
+def _status_clean(fa):
+    fa.fa_device_status()
+    yield
+    assert fa.fa_device_status() == 0, "a kernel wait timed out"
+
+
+def _run(fa, f8, dev):
+    u8 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+    p = f8.base
+    o, lse = fa.fwd_fp8(u8(f8.q8), u8(f8.k8), u8(f8.vt8), f32(f8.q_scale), f32(f8.k_scale), f32(f8.v_scale),
+                        causal=p.causal, scale=p.scale)
+    torch.cuda.synchronize(dev)
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def _check(o, lse, ref_o, ref_lse, bound_o, what):
+    assert np.all(np.isfinite(o)), what
+    inf = np.isneginf(ref_lse)
+    assert np.array_equal(np.isneginf(lse), inf), what + ": -inf LSE pattern"
+    assert np.all(o[inf] == 0.0), what
+    tol = 2.0 ** -4 * bound_o + 2.0 ** -8 * np.abs(ref_o) + 2e-3
+    err = np.abs(o - ref_o)
+    bad = err > tol
+    assert not bad.any(), "%s: %d elements over the bound, worst excess %.4g" % (what, bad.sum(), (err - tol).max())
+    fin = ~inf
+    if fin.any():
+        rel = np.abs(lse[fin] - ref_lse[fin]) / np.maximum(1.0, np.abs(ref_lse[fin]))
+        assert rel.max() <= LSE_RTOL, "%s: LSE %.3g" % (what, rel.max())
+
+
+FP8 = [
+    # (B, Hq, Hkv, Nq, Nk, causal); d = 128, Nk a multiple of 16
+    (1, 2, 2, 128, 128, False),
+    (1, 4, 2, 200, 256, False),     # GQA, ragged query tile
+    (2, 4, 2, 300, 304, True),      # causal, ragged tiles
+    (1, 2, 2, 130, 400, True),      # Nq < Nk, bottom-right
+    (1, 2, 2, 400, 208, True),      # Nq > Nk: early rows see no key
+    (1, 2, 1, 64, 16, False),       # one short K/V tile
+    (1, 8, 1, 640, 640, True),      # MQA, several units
+]
+
+
+@pytest.mark.parametrize("shape", FP8, ids=["-".join(map(str, s)) for s in FP8])
+def test_fp8_matches_oracle(fa, dev, shape):
+    B, Hq, Hkv, Nq, Nk, causal = shape
+    p = make_dense(B, Hq, Hkv, Nq, Nk, 128, seed=sum(shape) + 500, causal=causal, name="fp8")
+    f8 = make_fp8(p)
+    o, lse = _run(fa, f8, dev)
+    q, k, v = f8.dequantized()
+    ref_o, ref_lse = attention_fwd(q, k, v, p.scale, causal)
+    bound, _ = attention_fwd(q, k, np.abs(v), p.scale, causal)
+    _check(o, lse, ref_o, ref_lse, bound, "fp8 %s" % (shape,))
+
+
+def test_fp8_is_deterministic(fa, dev):
+    p = make_dense(1, 4, 2, 384, 384, 128, seed=91, causal=True)
+    f8 = make_fp8(p)
+    a = _run(fa, f8, dev)
+    b = _run(fa, f8, dev)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_fp8_headline_sampled(fa, dev):
+    """The B2 H32 N4096 d128 causal workload, quantized, on sampled rows."""
+    p = make_workload("b2_h32_n4096_d128_causal")
+    f8 = make_fp8(p)
+    o, lse = _run(fa, f8, dev)
+    q, k, v = f8.dequantized()
+    rng = np.random.default_rng(8)
+    samples = [(int(rng.integers(p.B)), int(rng.integers(p.Hq)), int(i))
+               for i in [0, 127, 128, 255, 4095, *rng.integers(p.Nq, size=35)]]
+    ref_o, ref_lse = attention_rows(q, k, v, p.scale, True, samples)
+    bound, _ = attention_rows(q, k, np.abs(v), p.scale, True, samples)
+    got_o = np.stack([o[b, h, i] for b, h, i in samples])
+    got_l = np.array([lse[b, h, i] for b, h, i in samples])
+    _check(got_o, got_l, ref_o, ref_lse, bound, "fp8 headline (sampled)")
