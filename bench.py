@@ -6,6 +6,10 @@ LSE) over the whole workload, i.e. one launch of the library's kernel.  The
 default workload is B=2, H=32, N=4096, d=128, causal.  FLOPs per step are
 4*B*H*Nq*Nk*d, halved for causal.
 
+With --fp8 a step is one forward pass of the 8-bit path (fa_fwd_fp8) on the
+workload quantized to e4m3 (V transposed); its roofline peak is the bf16 peak
+times the nominal fp8 : bf16 ratio of 2.
+
 With --bwd a step is instead one backward pass (dQ, dK, dV and delta from
 Q, K, V, O, LSE and dO: three kernel launches); FLOPs per step are counted
 as 2.5 times the forward's (the five products of the plain gradient), so the
@@ -38,6 +42,8 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd TFLOP/s bf16 (N=4096,d=128,causal) and % of dense-BF16 peak"
 METRIC_BWD = "attention bwd TFLOP/s bf16 (dQ, dK, dV; 2.5x the forward FLOPs) and % of dense-BF16 peak"
+METRIC_FP8 = "attention fwd TFLOP/s fp8 e4m3 (d=128) and % of dense-FP8 peak"
+FP8_OVER_BF16 = 2.0   # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
@@ -63,6 +69,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--bwd", action="store_true", help="time the backward pass instead of the forward")
+    ap.add_argument("--fp8", action="store_true", help="time the 8-bit (e4m3) forward")
     return ap.parse_args(argv)
 
 
@@ -268,8 +275,8 @@ def run_reference(args):
     from fa_inputs import make_workload, HEADLINE
     name = args.workload or HEADLINE
     prob = make_workload(name)
-    if args.bwd and prob.varlen:
-        raise SystemExit("--bwd: dense workloads only")
+    if (args.bwd or args.fp8) and prob.varlen:
+        raise SystemExit("--bwd / --fp8: dense workloads only")
     per_step = max(1.0, args.cpu_budget_s / max(1, args.steps))
     for w in range(args.warmup):
         oracle_sample(prob, 0.0, start_head=w, backward=args.bwd)
@@ -283,7 +290,8 @@ def run_reference(args):
         descs.append(desc)
     wall = time.perf_counter() - t0
     value = statistics.mean(vals)
-    line = {"metric": METRIC_BWD if args.bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+    line = {"metric": METRIC_BWD if args.bwd else (METRIC_FP8 if args.fp8 else METRIC), "value": value,
+            "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -320,20 +328,28 @@ def run_ours(args):
     from fa_inputs import make_workload, make_dout, HEADLINE
     name = args.workload or HEADLINE
     prob = make_workload(name)
-    if args.bwd and prob.varlen:
-        raise SystemExit("--bwd: dense workloads only")
+    if (args.bwd or args.fp8) and prob.varlen:
+        raise SystemExit("--bwd / --fp8: dense workloads only")
     flops = prob.flops() * (2.5 if args.bwd else 1.0)
 
     def dev_bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
-    q0, k0, v0 = dev_bf16(prob.q), dev_bf16(prob.k), dev_bf16(prob.v)
+    if args.fp8:
+        from fa_inputs import make_fp8
+        f8 = make_fp8(prob)
+        u8 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+        f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+        q0, k0, v0 = u8(f8.q8), u8(f8.k8), u8(f8.vt8)
+        descales = (f32(f8.q_scale), f32(f8.k_scale), f32(f8.v_scale))
+    else:
+        q0, k0, v0 = dev_bf16(prob.q), dev_bf16(prob.k), dev_bf16(prob.v)
     do0 = dev_bf16(make_dout(prob, 1000)) if args.bwd else None
     cu = None if prob.cu_seqlens is None else torch.from_numpy(prob.cu_seqlens).to(dev)
     sets = []
     for r in range(ROTATE):
         q, k, v = (q0, k0, v0) if r == 0 else (q0.clone(), k0.clone(), v0.clone())
-        o = torch.empty_like(q)
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
         if args.bwd:
             # The forward pass's O and LSE are inputs of the backward step.
@@ -355,6 +371,9 @@ def run_ours(args):
                    dq=dq, dk=dk, dv=dv, delta=dl)
             return
         q, k, v, o, lse = sets[i % ROTATE]
+        if args.fp8:
+            fa.fwd_fp8(q, k, v, *descales, causal=prob.causal, scale=prob.scale, out=o, lse=lse, stream=stream)
+            return
         fa.fwd(q, k, v, causal=prob.causal, scale=prob.scale, cu_seqlens=cu, out=o, lse=lse, stream=stream)
 
     fa.fa_device_status()
@@ -406,6 +425,8 @@ def run_ours(args):
         if args.bwd:
             fa.bwd(q, k, v, o, lse, do, causal=prob.causal, scale=prob.scale, stream=stream,
                    dq=dq, dk=dk, dv=dv, delta=dl)
+        elif args.fp8:
+            fa.fwd_fp8(q, k, v, *descales, causal=prob.causal, scale=prob.scale, out=o, lse=lse, stream=stream)
         else:
             fa.fwd(q, k, v, causal=prob.causal, scale=prob.scale, cu_seqlens=cu, out=o, lse=lse, stream=stream)
         for dst, src in zip(houts, outs):
@@ -441,6 +462,17 @@ def run_ours(args):
                     "kernel": "fa_bwd", "algorithmic_flop_per_launch": flops,
                     "executed_flop_per_launch": prob.flops() * 3.5,
                     "note": "one step = bwd_delta_kernel + bwd_dq_kernel + bwd_dkdv_kernel"}
+    elif args.fp8:
+        achieved = flops / launch_s / 1e12
+        sustained = ms_total >= 1000.0
+        peak = FP8_OVER_BF16 * (peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"])
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": load_traffic(name + ":fp8"),
+                    "peak_kind": "fp8 dense %s = bf16 %s x %.0f (nominal fp8:bf16 ratio)"
+                                 % ("sustained" if sustained else "burst", tag, FP8_OVER_BF16),
+                    "kernel": "fa_fwd_kernel", "algorithmic_flop_per_launch": flops,
+                    "algorithmic_bytes_per_launch": prob.q.size + prob.k.size + prob.v.size + 2 * prob.q.size
+                                                    + 4 * (prob.q.size // prob.d)}
     elif is_decode(prob):
         # Split-KV path: bound by reading K and V from HBM.
         achieved = prob.io_bytes() / launch_s / 1e9
@@ -462,10 +494,11 @@ def run_ours(args):
                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                     "kernel": "fa_fwd_kernel", "algorithmic_flop_per_launch": flops,
                     "algorithmic_bytes_per_launch": prob.io_bytes()}
-    line = {"metric": METRIC_BWD if args.bwd else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+    line = {"metric": METRIC_BWD if args.bwd else (METRIC_FP8 if args.fp8 else METRIC), "value": value,
+            "unit": UNIT, "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "e4m3" if args.fp8 else "bf16", "data": "synthetic",
             "config": dict(workload_config(prob, name), parallelism="replicas" if world > 1 else "single",
                            l2="inputs rotated over %d copies (%.0f MB > %d MB L2)"
                               % (ROTATE, ROTATE * step_bytes / 1e6, L2_BYTES // 2 ** 20)),

@@ -96,6 +96,14 @@ constexpr int PREFETCH_KV_TILES = 3;
 #define FA_SOFT_EXP_PERIOD 0
 #endif
 constexpr int SOFT_EXP_PERIOD = FA_SOFT_EXP_PERIOD;
+// The same for the 8-bit path, whose products take half the tensor time, so
+// that its softmax is more often the limit.  Off as well: on GB300 one pair in
+// 4 (3, 2) made the B2/H32/N4096 causal 8-bit forward 24% (30%, 40%) slower;
+// its softmax warps are bound by instruction issue, not by the MUFU unit.
+#ifndef FA_SOFT_EXP_PERIOD_FP8
+#define FA_SOFT_EXP_PERIOD_FP8 0
+#endif
+constexpr int SOFT_EXP_PERIOD_FP8 = FA_SOFT_EXP_PERIOD_FP8;
 
 // Device status word: bit (1 << role) is set when that role gave up waiting.
 __device__ int g_fa_status;
@@ -683,8 +691,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int i = 0; i < 16; ++i) {
               const float2 x = fma2(make_float2(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nb2);
               float2 e;
-              if (SOFT_EXP_PERIOD > 0 && (i % (SOFT_EXP_PERIOD > 0 ? SOFT_EXP_PERIOD : 1)) == SOFT_EXP_PERIOD - 1 &&
-                  !need_mask)
+              constexpr int period = FP8 ? SOFT_EXP_PERIOD_FP8 : SOFT_EXP_PERIOD;
+              if (period > 0 && (i % (period > 0 ? period : 1)) == period - 1 && !need_mask)
                 e = exp2_soft2(x);  // no -inf here: the tile has no masked score
               else
                 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
