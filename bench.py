@@ -48,8 +48,7 @@ UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
     "fa_fwd_kernel": ["exact_attention_42_gb300/csrc/fa_fwd.cu", "exact_attention_42_gb300/csrc/ptx.cuh"],
-    "decode_kernel": ["exact_attention_42_gb300/csrc/fa_decode.cu", "exact_attention_42_gb300/csrc/fa_internal.h",
-                      "exact_attention_42_gb300/csrc/ptx.cuh"],
+    "decode_kernel": ["exact_attention_42_gb300/csrc/fa_decode.cu", "exact_attention_42_gb300/csrc/ptx.cuh"],
     "fa_bwd": ["exact_attention_42_gb300/csrc/fa_bwd.cu", "exact_attention_42_gb300/csrc/ptx.cuh"],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
