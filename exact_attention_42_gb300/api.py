@@ -107,28 +107,41 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
         dout: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
         stream: Optional[torch.cuda.Stream] = None, dq: Optional[torch.Tensor] = None,
         dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
-        delta: Optional[torch.Tensor] = None):
+        delta: Optional[torch.Tensor] = None, cu_seqlens: Optional[torch.Tensor] = None):
     """Gradients of exact attention on the GPU; returns (dQ, dK, dV, delta).
 
-    Dense layout only: q, o, dout [B, Hq, Nq, d], k/v [B, Hkv, Nk, d] bf16,
-    lse [B, Hq, Nq] fp32 from ``fwd`` on the same inputs.  delta [B, Hq, Nq]
-    fp32 is rowsum(dout * o).  Output tensors may be passed in (dq, dk, dv,
-    delta), otherwise they are allocated.  Runs on ``stream`` (default: the
-    current stream) without synchronising.
+    Dense: q, o, dout [B, Hq, Nq, d], k/v [B, Hkv, Nk, d] bf16, lse [B, Hq, Nq]
+    fp32 from ``fwd`` on the same inputs; delta [B, Hq, Nq] fp32 is
+    rowsum(dout * o).  Packed (cu_seqlens int32 [nseq+1] on the device): the
+    [H, T, d] / [H, T] layouts of ``fwd``.  Output tensors may be passed in
+    (dq, dk, dv, delta), otherwise they are allocated.  Runs on ``stream``
+    (default: the current stream) without synchronising.
     """
     dev = q.device
-    _check(q, "q", torch.bfloat16, 4, None)
+    packed = cu_seqlens is not None
+    nd = 3 if packed else 4
+    _check(q, "q", torch.bfloat16, nd, None)
     for t, n in ((k, "k"), (v, "v"), (o, "o"), (dout, "dout")):
-        _check(t, n, torch.bfloat16, 4, dev)
-    _check(lse, "lse", torch.float32, 3, dev)
-    B, Hq, Nq, d = q.shape
-    Bk, Hkv, Nk, dk_ = k.shape
-    if Bk != B or dk_ != d or tuple(v.shape) != tuple(k.shape):
-        raise ValueError("k and v must be [B, Hkv, Nk, d] with q's B and d")
+        _check(t, n, torch.bfloat16, nd, dev)
+    _check(lse, "lse", torch.float32, nd - 1, dev)
+    if packed:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, 1, dev)
+        Hq, Nq, d = q.shape
+        Hkv, Nk, dk_ = k.shape
+        B = cu_seqlens.numel() - 1
+        if Nk != Nq or dk_ != d or tuple(v.shape) != tuple(k.shape):
+            raise ValueError("packed k and v must be [Hkv, T, d] with q's T and d")
+        row_shape = (Hq, Nq)
+    else:
+        B, Hq, Nq, d = q.shape
+        Bk, Hkv, Nk, dk_ = k.shape
+        if Bk != B or dk_ != d or tuple(v.shape) != tuple(k.shape):
+            raise ValueError("k and v must be [B, Hkv, Nk, d] with q's B and d")
+        row_shape = (B, Hq, Nq)
     if tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
         raise ValueError("o and dout must have q's shape")
-    if tuple(lse.shape) != (B, Hq, Nq):
-        raise ValueError("lse must be [B, Hq, Nq]")
+    if tuple(lse.shape) != row_shape:
+        raise ValueError("lse must be %s" % (row_shape,))
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     def out(t, like, name, dtype=torch.bfloat16):
@@ -141,12 +154,12 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
     dq = out(dq, q.shape, "dq")
     dk = out(dk, k.shape, "dk")
     dv = out(dv, v.shape, "dv")
-    delta = out(delta, (B, Hq, Nq), "delta", torch.float32)
+    delta = out(delta, row_shape, "delta", torch.float32)
     with torch.cuda.device(dev):
         s = stream if stream is not None else torch.cuda.current_stream(dev)
         st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
                     dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(), B, Hq, Hkv, Nq, Nk, d,
-                    float(scale), int(bool(causal)), None, s.cuda_stream)
+                    float(scale), int(bool(causal)), cu_seqlens.data_ptr() if packed else None, s.cuda_stream)
     if st != 0:
         raise FaError(st, "fa_bwd")
     return dq, dk, dv, delta

@@ -156,8 +156,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream) {
   if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
   if (Hq % Hkv != 0) return FA_ERR_SHAPE;
+  if (cu_seqlens != nullptr && Nq != Nk) return FA_ERR_SHAPE;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
-  if (cu_seqlens != nullptr) return FA_ERR_UNSUPPORTED;
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_VALUE;
   if (B == 0 || Hq == 0 || Nq == 0) return FA_OK;
   if (q == nullptr || o == nullptr || dout == nullptr || lse == nullptr || dq == nullptr || delta == nullptr)
@@ -168,12 +168,13 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   if (Nk > 0 && (mis16(k) || mis16(v) || mis16(dk) || mis16(dv))) return FA_ERR_ALIGN;
   if ((reinterpret_cast<uintptr_t>(lse) & 3u) != 0 || (reinterpret_cast<uintptr_t>(delta) & 3u) != 0)
     return FA_ERR_ALIGN;
-  if (static_cast<long long>(B) * Hq > 0x7fffffffLL) return FA_ERR_SHAPE;
+  if (cu_seqlens != nullptr && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return FA_ERR_ALIGN;
+  if (cu_seqlens == nullptr && static_cast<long long>(B) * Hq > 0x7fffffffLL) return FA_ERR_SHAPE;
   fa::LaunchEnv env;
   const fa_status st = fa::launch_env(&env);
   if (st != FA_OK) return st;
-  return fa::launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream,
-                        env.sms, env.wait_limit_ns);
+  return fa::launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens,
+                        stream, env.sms, env.wait_limit_ns);
 }
 
 fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds) {

@@ -126,8 +126,9 @@ struct Params {
   float scale;
   float scale_log2;  // scale * log2(e)
   int causal;
-  int nqt, nkt;      // query / key tiles per head
-  int num_units;
+  int nqt, nkt;      // dense: query / key tiles per head
+  int num_units;     // dense: units of the launched kernel; packed: computed on the device
+  const int* cu_seqlens;  // null: dense; else B+1 offsets of packed sequences (Nq == Nk == T)
   unsigned long long wait_limit_ns;
 };
 
@@ -212,24 +213,87 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
 // TMEM: [0,128) S   [128,256) dP   [256,256+D) dQ   [384,448) [448,512) dS x2
 // ---------------------------------------------------------------------------
 
-// Unit u -> (batch*head, query tile); later query tiles (more visible keys
-// under a causal mask) first, so the static schedule deals the heaviest
-// units first.  (Dealing them by groups of heads instead, so that concurrent
-// CTAs share K/V in L2, cut DRAM reads threefold on GB300 but not the time,
-// and slowed the dK/dV kernel by unbalancing the schedule.)
-__device__ __forceinline__ void dq_unit(const Params& p, int u, int& bh, int& qt) {
-  const int bh_count = p.B * p.Hq;
-  qt = p.nqt - 1 - u / bh_count;
-  bh = u % bh_count;
+__device__ __forceinline__ int clampi(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
+
+// Units of 128 rows over the sequences of a packed batch: sum of ceil(L/128).
+__device__ __forceinline__ int packed_tiles(const Params& p) {
+  const int T = p.Nq;
+  int prev = clampi(__ldg(p.cu_seqlens), 0, T), total = 0;
+  for (int s = 0; s < p.B; ++s) {
+    const int next = clampi(__ldg(p.cu_seqlens + s + 1), prev, T);
+    total += (next - prev + TILE - 1) / TILE;
+    prev = next;
+  }
+  return total;
 }
 
-// K/V tiles query tile qt must visit (0: no key visible to any of its rows).
-__device__ __forceinline__ int dq_kv_tiles(const Params& p, int qt) {
-  const int q0 = qt * TILE;
-  if (q0 >= p.Nq || p.Nk <= 0) return 0;
-  int last_key = p.Nk - 1;
+// Block blk of the packed batch's 128-row tiles, in sequence order: its
+// sequence's start token and length, and the tile's index in the sequence.
+__device__ __forceinline__ bool packed_block(const Params& p, int blk, int& start, int& len, int& tile, int& ntiles) {
+  const int T = p.Nq;
+  int prev = clampi(__ldg(p.cu_seqlens), 0, T);
+  for (int s = 0; s < p.B; ++s) {
+    const int next = clampi(__ldg(p.cu_seqlens + s + 1), prev, T);
+    const int nb = (next - prev + TILE - 1) / TILE;
+    if (blk < nb) {
+      start = prev;
+      len = next - prev;
+      tile = blk;
+      ntiles = nb;
+      return true;
+    }
+    blk -= nb;
+    prev = next;
+  }
+  return false;
+}
+
+// One unit of the dQ kernel: a 128-row query tile of one (sequence, head).
+// Rows of Q, dO, O, LSE, D and dQ are q_z * Nq + q_y + local row; rows of K
+// and V are k_z * Nk + k_y + local key (the tensor maps' head and row
+// coordinates).
+struct QUnit {
+  int Lq, Lk;  // query and key counts of the sequence
+  int row0;    // first query row of the tile, local to the sequence
+  int q_y, k_y, q_z, k_z;
+};
+
+// Dense: unit u -> (batch*head, query tile), later query tiles (more visible
+// keys under a causal mask) first, so the static schedule deals the heaviest
+// units first.  (Dealing them by groups of heads instead, so that concurrent
+// CTAs share K/V in L2, cut DRAM reads threefold on GB300 but not the time,
+// and slowed the dK/dV kernel by unbalancing the schedule.)  Packed: u =
+// blk * Hq + h over every sequence's tiles, a sequence's last tile first.
+__device__ __forceinline__ bool dq_unit(const Params& p, int u, QUnit& w) {
+  if (p.cu_seqlens == nullptr) {
+    const int bh_count = p.B * p.Hq;
+    const int qt = p.nqt - 1 - u / bh_count, bh = u % bh_count;
+    w.Lq = p.Nq;
+    w.Lk = p.Nk;
+    w.row0 = qt * TILE;
+    w.q_y = w.k_y = 0;
+    w.q_z = bh;
+    w.k_z = (bh / p.Hq) * p.Hkv + (bh % p.Hq) / p.group;
+    return true;
+  }
+  const int h = u % p.Hq;
+  int start, len, tile, nb;
+  if (!packed_block(p, u / p.Hq, start, len, tile, nb)) return false;
+  w.Lq = w.Lk = len;
+  w.row0 = (nb - 1 - tile) * TILE;
+  w.q_y = w.k_y = start;
+  w.q_z = h;
+  w.k_z = h / p.group;
+  return true;
+}
+
+// K/V tiles the unit's query tile must visit (0: no key visible to any row).
+__device__ __forceinline__ int dq_kv_tiles(const Params& p, const QUnit& w) {
+  const int q0 = w.row0;
+  if (q0 >= w.Lq || w.Lk <= 0) return 0;
+  int last_key = w.Lk - 1;
   if (p.causal) {
-    last_key = min(last_key, min(q0 + TILE - 1, p.Nq - 1) + (p.Nk - p.Nq));
+    last_key = min(last_key, min(q0 + TILE - 1, w.Lq - 1) + (w.Lk - w.Lq));
     if (last_key < 0) return 0;
   }
   return last_key / TILE + 1;
@@ -241,6 +305,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const Params p) {
   using C = Cfg<D, false>;
+  constexpr bool KV_KERNEL = false;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -302,7 +367,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int num_units = p.num_units;
+  const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_tiles(p) * (KV_KERNEL ? p.Hkv : p.Hq);
   const int nrounds = (num_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
 
   if (warp == WARP_PRODUCER) {
@@ -318,16 +383,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int k = 0; k < nrounds && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= num_units) continue;
-        int bh, qt;
-        dq_unit(p, u, bh, qt);
-        const int nkv = dq_kv_tiles(p, qt);
+        QUnit w;
+        if (!dq_unit(p, u, w)) continue;
+        const int nkv = dq_kv_tiles(p, w);
         if (nkv == 0) continue;
-        const int b = bh / p.Hq, kvz = b * p.Hkv + (bh % p.Hq) / p.group;
         if (!(ok = wait_or_abort(qempty_bar, (qfills & 1u) ^ 1u, abort_flag, 0, p.wait_limit_ns))) break;
         mbar_arrive_expect_tx(qfull_bar, 2 * C::TILE_BYTES);
         for (int c = 0; c < C::CHUNKS; ++c) {
-          tma_load_3d(smem_u32(sQ) + c * C::CHUNK_BYTES, &tm_q, qfull_bar, c * 64, qt * TILE, bh);
-          tma_load_3d(smem_u32(sDO) + c * C::CHUNK_BYTES, &tm_do, qfull_bar, c * 64, qt * TILE, bh);
+          tma_load_3d(smem_u32(sQ) + c * C::CHUNK_BYTES, &tm_q, qfull_bar, c * 64, w.q_y + w.row0, w.q_z);
+          tma_load_3d(smem_u32(sDO) + c * C::CHUNK_BYTES, &tm_do, qfull_bar, c * 64, w.q_y + w.row0, w.q_z);
         }
         ++qfills;
         for (int j = 0; j < nkv && ok; ++j) {
@@ -338,7 +402,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
             const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
             for (int c = 0; c < C::CHUNKS; ++c)
-              tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, full_bar(s), c * 64, j * TILE, kvz);
+              tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, full_bar(s), c * 64, w.k_y + j * TILE,
+                          w.k_z);
             ++it;
           }
         }
@@ -368,9 +433,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int k = 0; k < nrounds && ok; ++k) {
       const int u = snake_unit(k);
       if (u >= num_units) continue;
-      int bh, qt;
-      dq_unit(p, u, bh, qt);
-      const int nkv = dq_kv_tiles(p, qt);
+      QUnit w;
+      if (!dq_unit(p, u, w)) continue;
+      const int nkv = dq_kv_tiles(p, w);
       if (nkv == 0) continue;
       if (!(ok = wait_or_abort(qfull_bar, qcnt & 1u, abort_flag, 1, p.wait_limit_ns))) break;
       ++qcnt;
@@ -453,12 +518,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int k = 0; k < nrounds && ok; ++k) {
       const int u = snake_unit(k);
       if (u >= num_units) continue;
-      int bh, qt;
-      dq_unit(p, u, bh, qt);
-      const int nkv = dq_kv_tiles(p, qt);
-      const int row = qt * TILE + r;
-      const bool row_ok = row < p.Nq;
-      const long long grow = static_cast<long long>(bh) * p.Nq + row;
+      QUnit w;
+      if (!dq_unit(p, u, w)) continue;
+      const int nkv = dq_kv_tiles(p, w);
+      const int row = w.row0 + r;
+      const bool row_ok = row < w.Lq;
+      const long long grow = static_cast<long long>(w.q_z) * p.Nq + w.q_y + row;
       if (nkv == 0) {
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(p.dq + grow * D + (D / 2) * h);
@@ -469,7 +534,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       const float lse2 = row_ok ? __ldg(p.lse + grow) * LOG2E : INFINITY;
       const float dlt = row_ok ? __ldg(p.delta + grow) : 0.f;
-      const int lim = row_ok ? (p.causal ? min(p.Nk - 1, row + (p.Nk - p.Nq)) : (p.Nk - 1)) : -1;
+      const int lim = row_ok ? (p.causal ? min(w.Lk - 1, row + (w.Lk - w.Lq)) : (w.Lk - 1)) : -1;
       const float2 c2 = make_float2(sl2, sl2), nl2 = make_float2(-lse2, -lse2), dl2 = make_float2(dlt, dlt);
       for (int j = 0; j < nkv; ++j) {
         const uint32_t g = gt + j;
@@ -571,20 +636,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // over scores it has already read.
 // ---------------------------------------------------------------------------
 
-// Unit u -> (batch*kv head, key tile); the first key tiles (read by the most
-// query tiles under a causal mask) come first.
-__device__ __forceinline__ void kv_unit(const Params& p, int u, int& bkv, int& kt) {
-  const int n = p.B * p.Hkv;
-  kt = u / n;
-  bkv = u % n;
+// One unit of the dK/dV kernel: a 128-key tile of one (sequence, key/value
+// head), with every query tile of the head's query group that sees it.  Row
+// coordinates as for QUnit; the group's query heads are q_z0 .. q_z0+group-1.
+struct KUnit {
+  int Lq, Lk;  // query and key counts of the sequence
+  int key0;    // first key of the tile, local to the sequence
+  int q_y, k_y, q_z0, k_z;
+};
+
+// Dense: unit u -> (batch*kv head, key tile); the first key tiles (read by the
+// most query tiles under a causal mask) come first.  Packed: u = blk * Hkv +
+// kvh over every sequence's tiles, a sequence's first key tile first.
+__device__ __forceinline__ bool kv_unit(const Params& p, int u, KUnit& w) {
+  if (p.cu_seqlens == nullptr) {
+    const int n = p.B * p.Hkv;
+    const int kt = u / n, bkv = u % n;
+    w.Lq = p.Nq;
+    w.Lk = p.Nk;
+    w.key0 = kt * TILE;
+    w.q_y = w.k_y = 0;
+    w.k_z = bkv;
+    w.q_z0 = (bkv / p.Hkv) * p.Hq + (bkv % p.Hkv) * p.group;
+    return true;
+  }
+  const int kvh = u % p.Hkv;
+  int start, len, tile, nb;
+  if (!packed_block(p, u / p.Hkv, start, len, tile, nb)) return false;
+  w.Lq = w.Lk = len;
+  w.key0 = tile * TILE;
+  w.q_y = w.k_y = start;
+  w.k_z = kvh;
+  w.q_z0 = kvh * p.group;
+  return true;
 }
 
-// First query tile that sees any key of key tile kt (nqt: none).
-__device__ __forceinline__ int kv_first_qtile(const Params& p, int kt) {
+// Query tiles of the unit's sequence, and the first that sees any key of the
+// unit's key tile (the tile count: none).
+__device__ __forceinline__ int kv_query_tiles(const KUnit& w) { return (w.Lq + TILE - 1) / TILE; }
+__device__ __forceinline__ int kv_first_qtile(const Params& p, const KUnit& w) {
+  const int nq = kv_query_tiles(w);
   if (!p.causal) return 0;
-  const int q_min = kt * TILE - (p.Nk - p.Nq);  // first query row whose diagonal reaches key kt*TILE
+  const int q_min = w.key0 - (w.Lk - w.Lq);  // first query row whose diagonal reaches key key0
   if (q_min <= 0) return 0;
-  if (q_min >= p.Nq) return p.nqt;
+  if (q_min >= w.Lq) return nq;
   return q_min / TILE;
 }
 
@@ -594,6 +689,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const Params p) {
   using C = Cfg<D, true>;
+  constexpr bool KV_KERNEL = true;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -655,7 +751,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int num_units = p.num_units;
+  const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_tiles(p) * (KV_KERNEL ? p.Hkv : p.Hq);
   const int nrounds = (num_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
 
   if (warp == WARP_PRODUCER) {
@@ -669,21 +765,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int k = 0; k < nrounds && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= num_units) continue;
-        int bkv, kt;
-        kv_unit(p, u, bkv, kt);
-        const int i0 = kv_first_qtile(p, kt);
-        if (i0 >= p.nqt) continue;
+        KUnit w;
+        if (!kv_unit(p, u, w)) continue;
+        const int i0 = kv_first_qtile(p, w), nq = kv_query_tiles(w);
+        if (i0 >= nq) continue;
         if (!(ok = wait_or_abort(kvempty_bar, (kvfills & 1u) ^ 1u, abort_flag, 4, p.wait_limit_ns))) break;
         mbar_arrive_expect_tx(kvfull_bar, 2 * C::TILE_BYTES);
         for (int c = 0; c < C::CHUNKS; ++c) {
-          tma_load_3d(smem_u32(sK) + c * C::CHUNK_BYTES, &tm_k, kvfull_bar, c * 64, kt * TILE, bkv);
-          tma_load_3d(smem_u32(sV) + c * C::CHUNK_BYTES, &tm_v, kvfull_bar, c * 64, kt * TILE, bkv);
+          tma_load_3d(smem_u32(sK) + c * C::CHUNK_BYTES, &tm_k, kvfull_bar, c * 64, w.k_y + w.key0, w.k_z);
+          tma_load_3d(smem_u32(sV) + c * C::CHUNK_BYTES, &tm_v, kvfull_bar, c * 64, w.k_y + w.key0, w.k_z);
         }
         ++kvfills;
-        const int b = bkv / p.Hkv, kvh = bkv % p.Hkv;
         for (int hg = 0; hg < p.group && ok; ++hg) {
-          const int qz = b * p.Hq + kvh * p.group + hg;
-          for (int i = i0; i < p.nqt && ok; ++i) {
+          const int qz = w.q_z0 + hg;
+          for (int i = i0; i < nq && ok; ++i) {
             for (int x = 0; x < 2; ++x) {
               const int s = it % C::NS;
               if (!(ok = wait_or_abort(empty_bar(s), ((it / C::NS) & 1u) ^ 1u, abort_flag, 4, p.wait_limit_ns)))
@@ -691,7 +786,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
               const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
               for (int c = 0; c < C::CHUNKS; ++c)
-                tma_load_3d(dst + c * C::CHUNK_BYTES, x ? &tm_do : &tm_q, full_bar(s), c * 64, i * TILE, qz);
+                tma_load_3d(dst + c * C::CHUNK_BYTES, x ? &tm_do : &tm_q, full_bar(s), c * 64, w.q_y + i * TILE,
+                            qz);
               ++it;
             }
           }
@@ -721,11 +817,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int k = 0; k < nrounds && ok; ++k) {
       const int u = snake_unit(k);
       if (u >= num_units) continue;
-      int bkv, kt;
-      kv_unit(p, u, bkv, kt);
-      const int i0 = kv_first_qtile(p, kt);
-      if (i0 >= p.nqt) continue;
-      const int ntiles = p.group * (p.nqt - i0);
+      KUnit w;
+      if (!kv_unit(p, u, w)) continue;
+      const int i0 = kv_first_qtile(p, w), nq = kv_query_tiles(w);
+      if (i0 >= nq) continue;
+      const int ntiles = p.group * (nq - i0);
       if (!(ok = wait_or_abort(kvfull_bar, kvcnt & 1u, abort_flag, 5, p.wait_limit_ns))) break;
       ++kvcnt;
       // Products of the unit's query tile t (global tile g = gt + t); Q(t)
@@ -805,19 +901,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tS = tmem + lane_base + 64 * h;
     const uint32_t tDP = tmem + lane_base + 128 + 64 * h;
     const float sl2 = p.scale_log2;
-    const int shift = p.Nk - p.Nq;
     uint32_t gt = 0, units_done = 0;
     bool ok = true;
     for (int k = 0; k < nrounds && ok; ++k) {
       const int u = snake_unit(k);
       if (u >= num_units) continue;
-      int bkv, kt;
-      kv_unit(p, u, bkv, kt);
-      const int i0 = kv_first_qtile(p, kt);
-      const int key = kt * TILE + r;
-      const bool key_ok = key < p.Nk;
-      const long long krow = static_cast<long long>(bkv) * p.Nk + key;
-      if (i0 >= p.nqt) {
+      KUnit w;
+      if (!kv_unit(p, u, w)) continue;
+      const int i0 = kv_first_qtile(p, w), nq = kv_query_tiles(w);
+      const int key = w.key0 + r;
+      const bool key_ok = key < w.Lk;
+      const long long krow = static_cast<long long>(w.k_z) * p.Nk + w.k_y + key;
+      if (i0 >= nq) {
         if (key_ok) {
           uint4* dk = reinterpret_cast<uint4*>(p.dk + krow * D + (D / 2) * h);
           uint4* dv = reinterpret_cast<uint4*>(p.dv + krow * D + (D / 2) * h);
@@ -826,16 +921,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         continue;
       }
-      const int b = bkv / p.Hkv, kvh = bkv % p.Hkv;
-      const int per_head = p.nqt - i0;
+      const int per_head = nq - i0;
       const int ntiles = p.group * per_head;
-      // Tile t covers query head kvh*group + t/per_head, query tile i0 + t%per_head.
+      // Tile t covers query head q_z0 + t/per_head, query tile i0 + t%per_head.
       auto vec_value = [&](int t) -> float {
-        const int qh = kvh * p.group + t / per_head;
         const int q = (i0 + t % per_head) * TILE + (tt & 127);
-        const long long qrow = (static_cast<long long>(b) * p.Hq + qh) * p.Nq + q;
-        if (tt < 128) return q < p.Nq ? -__ldg(p.lse + qrow) * LOG2E : -INFINITY;
-        return q < p.Nq ? __ldg(p.delta + qrow) : 0.f;
+        const long long qrow = static_cast<long long>(w.q_z0 + t / per_head) * p.Nq + w.q_y + q;
+        if (tt < 128) return q < w.Lq ? -__ldg(p.lse + qrow) * LOG2E : -INFINITY;
+        return q < w.Lq ? __ldg(p.delta + qrow) : 0.f;
       };
       float v_next = vec_value(0);
       for (int t = 0; t < ntiles; ++t) {
@@ -853,8 +946,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // Query column c is visible to this key iff the query exists
         // (c <= qmax) and, under the causal mask, the key is on or left of
         // the query's diagonal (c >= cmin).
-        const int qmax = p.Nq - 1 - q0;
-        const int cmin = p.causal ? key - shift - q0 : -0x40000000;
+        const int qmax = w.Lq - 1 - q0;
+        const int cmin = p.causal ? key - (w.Lk - w.Lq) - q0 : -0x40000000;
         const float4* nlse4 = reinterpret_cast<const float4*>(vec + 64 * h);
         const float4* dlt4 = reinterpret_cast<const float4*>(vec + 128 + 64 * h);
         const float2 c2 = make_float2(sl2, sl2);
@@ -986,8 +1079,12 @@ int bwd_smem_bytes(int d) {  // the larger of the two main kernels
 template <int D>
 static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv,
-                              int Nq, int Nk, float scale, int causal, cudaStream_t stream, int sms,
-                              unsigned long long wait_limit_ns) {
+                              int Nq, int Nk, float scale, int causal, const int32_t* cu_seqlens,
+                              cudaStream_t stream, int sms, unsigned long long wait_limit_ns) {
+  const bool packed = cu_seqlens != nullptr;
+  // Tensor-map heads: (batch, head) pairs, or heads alone when packed.
+  const long long q_heads = packed ? Hq : static_cast<long long>(B) * Hq;
+  const long long kv_heads = packed ? Hkv : static_cast<long long>(B) * Hkv;
   using CQ = bwd::Cfg<D, false>;
   using CKV = bwd::Cfg<D, true>;
   static bool attr_set[kMaxDevicesDecode] = {};
@@ -1002,7 +1099,7 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
     attr_set[dev] = true;
   }
   // D = rowsum(dO * O) first: both main kernels read it.
-  const long long rows = static_cast<long long>(B) * Hq * Nq;
+  const long long rows = q_heads * Nq;
   {
     const long long threads = rows * (D / 8);
     const long long blocks = (threads + 255) / 256;
@@ -1014,11 +1111,11 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
   alignas(64) CUtensorMap tq, tdo, tk, tv;
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
-  if (!encode_bf16_rows_map(&tq, q, D, Nq, static_cast<long long>(B) * Hq, bwd::TILE) ||
-      !encode_bf16_rows_map(&tdo, dout, D, Nq, static_cast<long long>(B) * Hq, bwd::TILE))
+  if (!encode_bf16_rows_map(&tq, q, D, Nq, q_heads, bwd::TILE) ||
+      !encode_bf16_rows_map(&tdo, dout, D, Nq, q_heads, bwd::TILE))
     return FA_ERR_CUDA;
-  if (Nk > 0 && (!encode_bf16_rows_map(&tk, k, D, Nk, static_cast<long long>(B) * Hkv, bwd::TILE) ||
-                 !encode_bf16_rows_map(&tv, v, D, Nk, static_cast<long long>(B) * Hkv, bwd::TILE)))
+  if (Nk > 0 && (!encode_bf16_rows_map(&tk, k, D, Nk, kv_heads, bwd::TILE) ||
+                 !encode_bf16_rows_map(&tv, v, D, Nk, kv_heads, bwd::TILE)))
     return FA_ERR_CUDA;
   bwd::Params prm;
   prm.q = static_cast<const __nv_bfloat16*>(q);
@@ -1041,11 +1138,15 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
   prm.nqt = (Nq + bwd::TILE - 1) / bwd::TILE;
   prm.nkt = (Nk + bwd::TILE - 1) / bwd::TILE;
   prm.wait_limit_ns = wait_limit_ns;
-  // dQ: one unit per (batch, query head, query tile).
+  prm.cu_seqlens = cu_seqlens;
+  // Packed: the units are counted on the device; every sequence adds at most
+  // one partial tile, which bounds the grid.
+  const long long tiles_bound = packed ? (Nq + bwd::TILE - 1) / bwd::TILE + B : 0;
+  // dQ: one unit per (batch or sequence, query head, query tile).
   {
-    const long long units = static_cast<long long>(B) * Hq * prm.nqt;
+    const long long units = packed ? Hq * tiles_bound : static_cast<long long>(B) * Hq * prm.nqt;
     if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
-    prm.num_units = static_cast<int>(units);
+    prm.num_units = packed ? -1 : static_cast<int>(units);
     const long long grid = units < sms ? units : sms;
     if (grid > 0) {
       bwd::bwd_dq_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, CQ::SMEM_BYTES, stream>>>(tq, tdo, tk,
@@ -1053,11 +1154,11 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
       if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     }
   }
-  // dK, dV: one unit per (batch, key/value head, key tile).
+  // dK, dV: one unit per (batch or sequence, key/value head, key tile).
   {
-    const long long units = static_cast<long long>(B) * Hkv * prm.nkt;
+    const long long units = packed ? Hkv * tiles_bound : static_cast<long long>(B) * Hkv * prm.nkt;
     if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
-    prm.num_units = static_cast<int>(units);
+    prm.num_units = packed ? -1 : static_cast<int>(units);
     const long long grid = units < sms ? units : sms;
     if (grid > 0) {
       bwd::bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, CKV::SMEM_BYTES, stream>>>(
@@ -1070,12 +1171,13 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
 
 fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                      void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int Nq, int Nk, int d,
-                     float scale, int causal, cudaStream_t stream, int sms, unsigned long long wait_limit_ns) {
+                     float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream, int sms,
+                     unsigned long long wait_limit_ns) {
   if (d == 128)
-    return launch_bwd_t<128>(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, scale, causal, stream,
-                             sms, wait_limit_ns);
-  return launch_bwd_t<64>(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, scale, causal, stream, sms,
-                          wait_limit_ns);
+    return launch_bwd_t<128>(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens,
+                             stream, sms, wait_limit_ns);
+  return launch_bwd_t<64>(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens,
+                          stream, sms, wait_limit_ns);
 }
 
 }  // namespace fa

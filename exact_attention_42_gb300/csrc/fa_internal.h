@@ -46,10 +46,11 @@ fa_status launch_decode(const void* q, const void* k, const void* v, void* o, fl
 int decode_status_and_clear();  // -1 if the status word cannot be read
 int decode_smem_bytes(int d);
 
-// Backward pass (fa_bwd.cu), dense layout.
+// Backward pass (fa_bwd.cu), dense or packed layout.
 fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                      void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int Nq, int Nk, int d,
-                     float scale, int causal, cudaStream_t stream, int sms, unsigned long long wait_limit_ns);
+                     float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream, int sms,
+                     unsigned long long wait_limit_ns);
 int bwd_status_and_clear();  // -1 if the status word cannot be read
 int bwd_smem_bytes(int d);
 

@@ -106,14 +106,15 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
  * and under grouped-query attention dK, dV of a key/value head are summed over
  * its Hq / Hkv query heads.  Masks and conventions are those of fa_fwd.
  *
- * Inputs (device, row-major, contiguous):
+ * Inputs (device, row-major, contiguous), dense mode (cu_seqlens == NULL):
  *   q, o, dout [B, Hq, Nq, d] bf16     k, v [B, Hkv, Nk, d] bf16
  *   lse        [B, Hq, Nq]    fp32     (as written by fa_fwd for the same q, k, v)
  * Outputs (device, caller-allocated):
  *   dq [B, Hq, Nq, d] bf16, dk and dv [B, Hkv, Nk, d] bf16,
  *   delta [B, Hq, Nq] fp32: the per-row statistic rowsum(dout * o).
- * cu_seqlens must be NULL: the packed layout is not supported by the backward
- * pass (FA_ERR_UNSUPPORTED).
+ * Packed mode (cu_seqlens != NULL, as for fa_fwd): q, o, dout, dq [Hq, T, d],
+ * k, v, dk, dv [Hkv, T, d], lse and delta [Hq, T], Nq == Nk == T; each
+ * sequence's gradients involve only its own tokens.
  *
  * Three kernels are enqueued (delta, then dQ, then dK/dV); the library
  * allocates nothing and uses no atomics, so results are deterministic.

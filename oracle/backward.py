@@ -62,13 +62,30 @@ def _head_grads(qh, kh, vh, dob, rows, nq: int, scale: float, causal: bool):
     return dq, dk, dv, dlt
 
 
-def attention_bwd(q, k, v, do, scale: float, causal: bool):
-    """Gradients of exact attention in float64 (dense layout).
+def attention_bwd(q, k, v, do, scale: float, causal: bool, cu_seqlens=None):
+    """Gradients of exact attention in float64.
 
-    q, do: [B, Hq, Nq, d]; k, v: [B, Hkv, Nk, d].  Returns numpy float64
+    Dense: q, do [B, Hq, Nq, d]; k, v [B, Hkv, Nk, d].  Returns numpy float64
     arrays dq [B, Hq, Nq, d], dk and dv [B, Hkv, Nk, d], and the per-row
     statistic delta [B, Hq, Nq] = rowsum(dO * O).
+    Packed (``cu_seqlens`` [nseq+1]): q, do [Hq, T, d]; k, v [Hkv, T, d]; each
+    sequence attends only within itself, so its gradients are those of the
+    dense problem made of that sequence alone; returns dq [Hq, T, d], dk, dv
+    [Hkv, T, d] and delta [Hq, T].
     """
+    if cu_seqlens is not None:
+        q, k, v, do = (np.asarray(x, dtype=np.float64) for x in (q, k, v, do))
+        cu = [int(x) for x in np.asarray(cu_seqlens)]
+        dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        delta = np.zeros(q.shape[:2])
+        for s in range(len(cu) - 1):
+            t0, t1 = cu[s], cu[s + 1]
+            if t1 == t0:
+                continue
+            a, b_, c, d_ = attention_bwd(q[None, :, t0:t1], k[None, :, t0:t1], v[None, :, t0:t1],
+                                         do[None, :, t0:t1], scale, causal)
+            dq[:, t0:t1], dk[:, t0:t1], dv[:, t0:t1], delta[:, t0:t1] = a[0], b_[0], c[0], d_[0]
+        return dq, dk, dv, delta
     q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
     g = _check_shapes(q, k, v, None)
     assert do.shape == q.shape

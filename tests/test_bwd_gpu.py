@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 import torch
 
-from fa_inputs import bf16_bits_to_f64, make_dense, make_dout, make_workload
+from fa_inputs import bf16_bits_to_f64, make_dense, make_dout, make_varlen, make_workload
 from fa_testutil import to_dev
 from oracle import attention_bwd, attention_bwd_keys, attention_bwd_rows
 
@@ -131,3 +131,27 @@ def test_bwd_workload_sampled(fa, dev, name):
         rk, rv = attention_bwd_keys(q, k, v, do, prob.scale, prob.causal, b, kvh, keys)
         _check("dk[%d,%d]" % (b, kvh), dk[b, kvh, keys], rk)
         _check("dv[%d,%d]" % (b, kvh), dv[b, kvh, keys], rv)
+
+
+@pytest.mark.parametrize("lens,hq,hkv,d,causal", [
+    ([5, 130, 1, 256, 300], 4, 2, 128, True),
+    ([0, 129, 128, 64], 2, 2, 64, False),
+    ([700, 33], 4, 1, 128, True),
+])
+def test_bwd_varlen_matches_oracle(fa, dev, lens, hq, hkv, d, causal):
+    """Packed sequences (lengths 0, 1, ragged, tile multiples): every sequence's
+    gradients involve its own tokens only."""
+    prob = make_varlen(lens, hq, hkv, d, seed=sum(lens) + hq, causal=causal, name="bwd_varlen")
+    do_bits = make_dout(prob, sum(lens) + 7)
+    q, k, v, do = (to_dev(x, dev) for x in (prob.q, prob.k, prob.v, do_bits))
+    cu = torch.from_numpy(prob.cu_seqlens).to(dev)
+    o, lse = fa.fwd(q, k, v, causal=causal, scale=prob.scale, cu_seqlens=cu)
+    dq, dk, dv, delta = fa.bwd(q, k, v, o, lse, do, causal=causal, scale=prob.scale, cu_seqlens=cu)
+    torch.cuda.synchronize(dev)
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)
+    qq, kk, vv, dd = (bf16_bits_to_f64(x) for x in (prob.q, prob.k, prob.v, do_bits))
+    rq, rk, rv, rd = attention_bwd(qq, kk, vv, dd, prob.scale, causal, cu_seqlens=prob.cu_seqlens)
+    _check("dq", f(dq), rq)
+    _check("dk", f(dk), rk)
+    _check("dv", f(dv), rv)
+    _check("delta", f(delta), rd)

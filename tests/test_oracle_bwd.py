@@ -135,7 +135,39 @@ def pin_sampled_helpers():
     np.testing.assert_allclose(gv, dv[0, 1, keys], atol=1e-12)
 
 
-PINS = [("finite_differences", pin_finite_differences), ("autograd", pin_autograd),
+def pin_varlen_finite_differences():
+    """Packed sequences: finite differences of sum(O * dO) through the forward
+    oracle's own packed mode (sequences must not see each other)."""
+    lens = [3, 1, 4]
+    cu = np.array([0, 3, 4, 8], dtype=np.int32)
+    Hq, Hkv, d, T = 2, 1, 2, 8
+    q, k, v = _rand((Hq, T, d), 90), _rand((Hkv, T, d), 91), _rand((Hkv, T, d), 92)
+    do = _rand((Hq, T, d), 93)
+    scale = 0.8
+    for causal in (False, True):
+        dq, dk, dv, _ = attention_bwd(q, k, v, do, scale, causal, cu_seqlens=cu)
+
+        def loss(qq, kk, vv):
+            o, _ = attention_fwd(qq, kk, vv, scale, causal, cu_seqlens=cu)
+            return float((o * do).sum())
+        for grad, which in ((dq, 0), (dk, 1), (dv, 2)):
+            args = [q.copy(), k.copy(), v.copy()]
+            x = args[which]
+            fd = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                x0 = x[idx]
+                x[idx] = x0 + 1e-5
+                lp = loss(*args)
+                x[idx] = x0 - 1e-5
+                lm = loss(*args)
+                x[idx] = x0
+                fd[idx] = (lp - lm) / 2e-5
+            np.testing.assert_allclose(grad, fd, atol=1e-7, rtol=1e-6)
+    assert lens == [int(cu[i + 1] - cu[i]) for i in range(3)]
+
+
+PINS = [("finite_differences", pin_finite_differences), ("varlen_finite_differences", pin_varlen_finite_differences),
+        ("autograd", pin_autograd),
         ("single_key", pin_single_key), ("shift_invariants", pin_shift_invariants),
         ("sampled_helpers", pin_sampled_helpers)]
 
