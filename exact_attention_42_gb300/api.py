@@ -86,21 +86,69 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
 
 def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
              scale: Optional[float] = None, cu_seqlens: Optional[torch.Tensor] = None,
-             device: Optional[torch.device] = None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """The same call for host tensors: copies inputs to the GPU, runs ``fwd``,
-    copies O and LSE back to (pinned, when the inputs are pinned) host memory
-    and waits for the result."""
+             device: Optional[torch.device] = None, out: Optional[torch.Tensor] = None,
+             lse: Optional[torch.Tensor] = None, chunks: int = 4) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The forward for host tensors: copies the inputs to the GPU, runs the
+    kernel, copies O and LSE back to host memory and waits for the result.
+
+    Dense inputs are processed in about ``chunks`` pieces, each a contiguous
+    (batch, key/value head range) slice with its query heads.  Input copies,
+    kernels and output copies run on three streams, so the copies of one
+    piece overlap the kernel and the copies of others.  (On GB300 the
+    host-to-device copies of the B2/H32/N4096 inputs then bound the call.)  Inputs in pinned
+    memory make the copies asynchronous; ``out`` / ``lse`` (host tensors of
+    O's and LSE's shapes, pinned for overlap) receive the results, otherwise
+    they are allocated, pinned when the inputs are.  Packed batches, or
+    chunks <= 1, take one piece.
+    """
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     nb = q.is_pinned()
-    qd, kd, vd = (t.to(device, non_blocking=nb) for t in (q, k, v))
-    cud = None if cu_seqlens is None else cu_seqlens.to(device, non_blocking=nb)
-    o, lse = fwd(qd, kd, vd, causal=causal, scale=scale, cu_seqlens=cud)
-    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=nb)
-    lh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=nb)
-    oh.copy_(o, non_blocking=nb)
-    lh.copy_(lse, non_blocking=nb)
-    torch.cuda.current_stream(device).synchronize()
-    return oh, lh
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=nb)
+    if lse is None:
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, pin_memory=nb)
+    if cu_seqlens is not None or chunks <= 1 or q.dim() != 4:
+        qd, kd, vd = (t.to(device, non_blocking=nb) for t in (q, k, v))
+        cud = None if cu_seqlens is None else cu_seqlens.to(device, non_blocking=nb)
+        o, l = fwd(qd, kd, vd, causal=causal, scale=scale, cu_seqlens=cud)
+        out.copy_(o, non_blocking=nb)
+        lse.copy_(l, non_blocking=nb)
+        torch.cuda.current_stream(device).synchronize()
+        return out, lse
+    B, Hq, Nq, d = q.shape
+    Hkv = k.shape[1]
+    g = Hq // Hkv if Hkv > 0 else 1
+    per_b = max(1, -(-chunks // max(B, 1)))          # pieces per batch entry
+    kv_step = max(1, -(-Hkv // per_b))                # key/value heads per piece
+    pieces = [(b, h0, min(Hkv, h0 + kv_step)) for b in range(B) for h0 in range(0, Hkv, kv_step)]
+    with torch.cuda.device(device):
+        comp = torch.cuda.current_stream(device)
+        s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+        s_in.wait_stream(comp)
+        qd = torch.empty(q.shape, dtype=q.dtype, device=device)
+        kd = torch.empty(k.shape, dtype=k.dtype, device=device)
+        vd = torch.empty(v.shape, dtype=v.dtype, device=device)
+        od = torch.empty(q.shape, dtype=q.dtype, device=device)
+        ld = torch.empty(q.shape[:-1], dtype=torch.float32, device=device)
+        for b, h0, h1 in pieces:
+            qs, ks = (slice(b, b + 1), slice(h0 * g, h1 * g)), (slice(b, b + 1), slice(h0, h1))
+            with torch.cuda.stream(s_in):
+                qd[qs].copy_(q[qs], non_blocking=nb)
+                kd[ks].copy_(k[ks], non_blocking=nb)
+                vd[ks].copy_(v[ks], non_blocking=nb)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            comp.wait_event(ready)
+            fwd(qd[qs], kd[ks], vd[ks], causal=causal, scale=scale, out=od[qs], lse=ld[qs], stream=comp)
+            done = torch.cuda.Event()
+            done.record(comp)
+            s_out.wait_event(done)
+            with torch.cuda.stream(s_out):
+                out[qs].copy_(od[qs], non_blocking=nb)
+                lse[qs].copy_(ld[qs], non_blocking=nb)
+        s_out.synchronize()
+        comp.synchronize()
+    return out, lse
 
 
 def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,

@@ -35,7 +35,7 @@ int fwd_smem_bytes(int d);
 int fwd_threads();
 
 // Tensor map of a [heads, rows, d] bf16 tensor read in boxes of 64 columns x
-// box_rows rows with the 128-byte swizzle; false if the driver rejects it.
+// box_rows rows with the 128-byte swizzle; false if the CUDA driver rejects it.
 bool encode_bf16_rows_map(CUtensorMap* map, const void* base, int d, long long rows, long long heads, int box_rows);
 
 // Split-KV path (fa_decode.cu) for dense problems with (Hq / Hkv) * Nq <= 16.
