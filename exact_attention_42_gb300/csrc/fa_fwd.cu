@@ -57,7 +57,7 @@ constexpr int NQT = 2;            // query tiles per CTA
 constexpr int UNIT_ROWS = BLOCK_M * NQT;
 constexpr int NUM_THREADS = 384;  // three warpgroups
 constexpr int WARP_PRODUCER = 8;
-constexpr int WARP_MMA = 9;  // warps WARP_MMA + t issue the products of query tile t
+constexpr int WARP_MMA = 9;  // issues the products of both query tiles (warp 10 is idle)
 constexpr int WARP_QLOAD = 11;
 // Register split.  The kernel is launched at 168 registers per thread (the
 // most 12 warps allow: three warps share each sub-partition's 16K registers).
@@ -86,6 +86,16 @@ constexpr float P_SHIFT_FP8 = 8.0f;
 // the next unit's Q tiles and its first PREFETCH_KV_TILES K/V tiles.
 constexpr int PREFETCH_LEAD = 6;
 constexpr int PREFETCH_KV_TILES = 3;
+// The softmax hands P_t to the issuer in P_PARTS key ranges (1, 2 or 4), so
+// that the P V products of one range run while the next is exponentiated.
+// Two halves measured best on GB300: against one hand-over, +6% on the
+// B2/H32/N4096/d128 causal forward and +7% on GQA N16384; four quarters lose
+// the gain again to the extra TMEM store waits and barrier round trips.
+#ifndef FA_P_PARTS
+#define FA_P_PARTS 2
+#endif
+constexpr int P_PARTS = FA_P_PARTS;
+static_assert(P_PARTS == 1 || P_PARTS == 2 || P_PARTS == 4, "P_PARTS divides the four 32-key chunks");
 // Software exponentials: in tiles without a mask, one score pair in every
 // SOFT_EXP_PERIOD is exponentiated on the FMA/ALU pipes (exp2_soft2) instead
 // of the MUFU unit; 0 turns this off.  Off by default: on GB300 the MUFU unit
@@ -124,7 +134,7 @@ struct Cfg {
   static constexpr int SMEM_Q = NQT * TILE_BYTES;
   static constexpr int SMEM_RING = NS * TILE_BYTES;
   // barriers: full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int NUM_BARS = 2 * NS + 5 * NQT + 1;
+  static constexpr int NUM_BARS = 2 * NS + (4 + P_PARTS) * NQT + 1;
   static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + NUM_BARS * 8 + 16;
 };
 
@@ -315,7 +325,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto sfull_bar = [&](int t) { return bar_base + 8u * (2 * C::NS + 2 * NQT + t); };
   auto pfull_bar = [&](int t) { return bar_base + 8u * (2 * C::NS + 3 * NQT + t); };
   auto odone_bar = [&](int t) { return bar_base + 8u * (2 * C::NS + 4 * NQT + t); };
-  const uint32_t drain_bar = bar_base + 8u * (2 * C::NS + 5 * NQT);
+  // ppart_bar(t, i): keys [0, (i + 1) * BLOCK_N / P_PARTS) of P_t are in place (i < P_PARTS - 1).
+  auto ppart_bar = [&](int t, int i) { return bar_base + 8u * (2 * C::NS + (5 + i) * NQT + t); };
+  const uint32_t drain_bar = bar_base + 8u * (2 * C::NS + (4 + P_PARTS) * NQT);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -329,7 +341,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(qfull_bar(t), 1);
       mbar_init(qempty_bar(t), 1);
       mbar_init(sfull_bar(t), 1);
-      mbar_init(pfull_bar(t), BLOCK_M);
+      mbar_init(pfull_bar(t), BLOCK_M / 32);  // one arrival per softmax warp
+      for (int i = 0; i + 1 < P_PARTS; ++i) mbar_init(ppart_bar(t, i), BLOCK_M / 32);
       mbar_init(odone_bar(t), 1);
     }
     mbar_init(drain_bar, 1);
@@ -483,12 +496,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     };
     // O_t (+)= P_t V: P from TMEM (bf16 pairs), V MN-major (head dim contiguous), 16 keys per MMA.
-    auto issue_pv = [&](int t, int slot, bool accumulate) {
+    auto issue_pv = [&](int t, int slot, bool accumulate, int part) {
       if constexpr (FP8) {
         // V^T K-major (keys contiguous); P as packed e4m3 in TMEM, 8 columns per 32 keys.
         const uint64_t vt_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, 16, 1024);
 #pragma unroll
-        for (int kk = 0; kk < C::PV_KSTEPS; ++kk) {
+        for (int kk = part * C::PV_KSTEPS / P_PARTS; kk < (part + 1) * C::PV_KSTEPS / P_PARTS; ++kk) {
           if (leader)
             umma_ts_f8(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, vt_desc + static_cast<uint64_t>(kk * 32 >> 4),
                        IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
@@ -496,7 +509,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else {
         const uint64_t v_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
 #pragma unroll
-        for (int kk = 0; kk < BLOCK_N / 16; ++kk) {
+        for (int kk = part * BLOCK_N / (16 * P_PARTS); kk < (part + 1) * BLOCK_N / (16 * P_PARTS); ++kk) {
           if (leader)
             umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
                     v_desc + static_cast<uint64_t>(kk * 16 * 128 >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
@@ -556,10 +569,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
           if (!ok || j >= nkv[t]) continue;
-          if (!(ok = wait_or_abort(pfull_bar(t), pcnt[t] & 1u, abort_flag, 1, p.wait_limit_ns))) continue;
+          // P_t arrives in P_PARTS key ranges; the products of one range run
+          // while the softmax exponentiates the next.
+#pragma unroll
+          for (int i = 0; i < P_PARTS && ok; ++i) {
+            const uint32_t bar = (i + 1 < P_PARTS) ? ppart_bar(t, i) : pfull_bar(t);
+            if (!(ok = wait_or_abort(bar, pcnt[t] & 1u, abort_flag, 1, p.wait_limit_ns))) break;
+            tc_fence_after();
+            issue_pv(t, sv, j > 0 || i > 0, i);
+          }
+          if (!ok) continue;
           ++pcnt[t];
-          tc_fence_after();
-          issue_pv(t, sv, j > 0);
           if (j + 1 == nkv[t]) commit(odone_bar(t));  // last PV of this tile in the unit
           if (j + 1 < nkv[t]) {
             if (!k_ready) {
@@ -709,16 +729,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_st8(tS + c0 / 4, pk8);
           else
             tmem_st16(tS + c0 / 2, pk);
+          constexpr int CHUNKS_PER_PART = BLOCK_N / 32 / P_PARTS;
+          if ((c0 / 32 + 1) % CHUNKS_PER_PART == 0 && c0 + 32 < BLOCK_N) {  // a key range of P is in place
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ppart_bar(t, c0 / 32 / CHUNKS_PER_PART));
+          }
         }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pfull_bar(t));
         {
           const float2 a01 = add2(acc[0], acc[1]);
           const float2 a23 = add2(acc[2], acc[3]);
           const float2 a = add2(a01, a23);
           l += a.x + a.y;
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(pfull_bar(t));
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
