@@ -108,7 +108,7 @@ struct Cfg {
   static constexpr int SMEM_FIXED = 2 * TILE_BYTES;
   static constexpr int SMEM_RING = NS * TILE_BYTES;
   static constexpr int SMEM_VEC = KV ? 2 * 2 * TILE * 4 : 0;
-  static constexpr int NUM_BARS = 2 * NS + 12;
+  static constexpr int NUM_BARS = 2 * NS + 13;
   static constexpr int SMEM_BYTES = 1024 + SMEM_FIXED + SMEM_RING + SMEM_VEC + NUM_BARS * 8 + 16;
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
@@ -713,6 +713,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t p_full_bar = bar_base + 8u * (2 * C::NS + 3);
   const uint32_t dp_full_bar = bar_base + 8u * (2 * C::NS + 9);
   const uint32_t ds_full_bar = bar_base + 8u * (2 * C::NS + 10);
+  // The first 32 query columns of each warpgroup's P^T (dS^T) are in place.
+  const uint32_t p_half_bar = bar_base + 8u * (2 * C::NS + 11);
+  const uint32_t ds_half_bar = bar_base + 8u * (2 * C::NS + 12);
   const uint32_t dkv_done_bar = bar_base + 8u * (2 * C::NS + 4);
   const uint32_t dkv_free_bar = bar_base + 8u * (2 * C::NS + 5);
   const uint32_t drain_bar = bar_base + 8u * (2 * C::NS + 6);
@@ -736,6 +739,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(p_full_bar, SOFTMAX_WARPS);
     mbar_init(dp_full_bar, 1);
     mbar_init(ds_full_bar, SOFTMAX_WARPS);
+    mbar_init(p_half_bar, SOFTMAX_WARPS);
+    mbar_init(ds_half_bar, SOFTMAX_WARPS);
     mbar_init(dkv_done_bar, 1);
     mbar_init(dkv_free_bar, SOFTMAX_WARPS);
     mbar_init(drain_bar, 1);
@@ -858,22 +863,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         return true;
       };
       // dV += P^T dO(t) and dK += dS^T Q(t): A from TMEM (warpgroup w's query
-      // pairs at columns 64 w + 8 (kk % 4)), B MN-major from the ring.
+      // pairs at columns 64 w + 8 (kk % 4)), B MN-major from the ring.  The
+      // softmax hands each operand over in two halves: query columns 0-31 of
+      // both warpgroups (k-steps 0, 1, 4, 5) run while it computes 32-63.
       auto issue_grad = [&](int t, bool dk) -> bool {
         const uint32_t g = gt + t, f = it0 + 2 * t + (dk ? 0 : 1);
-        if (!wait_or_abort(dk ? ds_full_bar : p_full_bar, g & 1u, abort_flag, 5, p.wait_limit_ns)) return false;
-        if (!dk && t == 0 && units_done > 0 &&
-            !wait_or_abort(dkv_free_bar, (units_done - 1) & 1u, abort_flag, 5, p.wait_limit_ns))
-          return false;
-        tc_fence_after();
         const uint64_t b_mn = smem_desc_sw128(ring_addr + (f % C::NS) * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
         const uint32_t d_col = dk ? 384 : 256, a_col = dk ? 128 : 0;
 #pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk) {
-          const uint32_t acol = a_col + 64 * (kk / 4) + 8 * (kk % 4);
-          if (leader)
-            umma_ts(tmem + d_col, tmem + acol, b_mn + (static_cast<uint64_t>(kk * 16 * 128) >> 4), IDESC_G,
-                    (t > 0 || kk > 0) ? 1u : 0u);
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t bar = part == 0 ? (dk ? ds_half_bar : p_half_bar) : (dk ? ds_full_bar : p_full_bar);
+          if (!wait_or_abort(bar, g & 1u, abort_flag, 5, p.wait_limit_ns)) return false;
+          if (part == 0 && !dk && t == 0 && units_done > 0 &&
+              !wait_or_abort(dkv_free_bar, (units_done - 1) & 1u, abort_flag, 5, p.wait_limit_ns))
+            return false;
+          tc_fence_after();
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kk = 4 * (k4 / 2) + 2 * part + (k4 % 2);  // part 0: 0, 1, 4, 5; part 1: 2, 3, 6, 7
+            const uint32_t acol = a_col + 64 * (kk / 4) + 8 * (kk % 4);
+            if (leader)
+              umma_ts(tmem + d_col, tmem + acol, b_mn + (static_cast<uint64_t>(kk * 16 * 128) >> 4), IDESC_G,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         commit(empty_bar(f % C::NS));  // dO(t) after dV, Q(t) after dK
         return true;
@@ -982,6 +994,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           tmem_st16(tS + 16 * half, ppk);
+          if (half == 0) {
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(p_half_bar);
+          }
         }
         tmem_wait_st();
         tc_fence_before();
@@ -1008,6 +1025,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           tmem_st16(tDP + 16 * half, dpk);
+          if (half == 0) {
+            tmem_wait_st();
+            tc_fence_before();
+            warp_arrive(ds_half_bar);
+          }
         }
         tmem_wait_st();
         tc_fence_before();
