@@ -76,16 +76,18 @@ static_assert(2 * REG_SOFTMAX + REG_OTHER <= 512, "register split exceeds a sub-
 constexpr float TAU = 8.0f;
 // 8-bit path: P is stored as e4m3 (largest finite 448, smallest subnormal
 // 2^-9).  There the reference max moves when a row max exceeds it by more
-// than TAU_FP8 and p is taken as 2^(s - m + P_SHIFT_FP8), so that
-// 0 < p <= 2^(TAU_FP8 + P_SHIFT_FP8) = 256 and only terms below 2^-15 of the
-// row max (2^-17 when the reference is 2 behind) are lost to underflow; l
-// carries the same factor, which O / l cancels and the LSE subtracts.  With
-// threshold 0 the warp-wide O correction ran on most early K/V tiles; 2
-// made the B2/H32/N4096/d128 causal 8-bit forward 6.5% faster (threshold 1
-// with shift 7: 2.4%).
-constexpr float TAU_FP8 = 2.0f;
-constexpr float P_SHIFT_FP8 = 6.0f;
-static_assert(TAU_FP8 + P_SHIFT_FP8 <= 8.0f, "p must stay below the largest finite e4m3 value, 448");
+// than TAU_FP8, and p is taken as 2^(s - m + P_SHIFT_FP8), so that
+// 0 < p <= 2^(TAU_FP8 + P_SHIFT_FP8) = 2^8.75 ~ 430.5 < 448.  Terms below
+// 2^-14 of the reference (2^-14 to 2^-17.75 of the row max) underflow to 0;
+// l carries the same factor, which O / l cancels and the LSE subtracts.
+// The warp-wide O correction runs whenever any of a warp's 32 rows moves its
+// reference, so the threshold sets how often it runs.  Against threshold 0
+// with a 2^8 scale, threshold 2 (scale 2^6) made the B2/H32/N4096/d128 causal
+// 8-bit forward 6.5% faster, 2.75 (2^6) 13%, and 3.75 (2^5) 16%; the error
+// against the oracle did not change.
+constexpr float TAU_FP8 = 3.75f;
+constexpr float P_SHIFT_FP8 = 5.0f;
+static_assert(TAU_FP8 + P_SHIFT_FP8 <= 8.75f, "p must stay below the largest finite e4m3 value, 448");
 // L2 prefetch of the next unit: issued when the producer starts loading the
 // K/V tile PREFETCH_LEAD tiles before the end of the current unit, covering
 // the next unit's Q tiles and its first PREFETCH_KV_TILES K/V tiles.
