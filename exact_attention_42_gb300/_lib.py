@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_fp8.restype = ci
             L.fa_bwd_smem_bytes.argtypes = [ci]
             L.fa_bwd_smem_bytes.restype = ci
+            L.fa_fp8_quantize.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp, vp]
+            L.fa_fp8_quantize.restype = ci
             _lib = L
     return _lib
 
@@ -87,6 +89,11 @@ def fa_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv,
     """Direct call of the 8-bit forward entry point with integer addresses; returns the status."""
     return lib().fa_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, Nq, Nk, d,
                             ctypes.c_float(scale), int(causal), stream)
+
+
+def fa_fp8_quantize(x, x8, descale, B, H, N, d, transpose, signs, stream) -> int:
+    """Direct call of the e4m3 quantization entry point with integer addresses; returns the status."""
+    return lib().fa_fp8_quantize(x, x8, descale, B, H, N, d, int(transpose), signs, stream)
 
 
 def fa_status_string(status: int) -> str:

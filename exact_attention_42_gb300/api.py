@@ -10,7 +10,7 @@ from typing import Optional, Tuple
 
 import torch
 
-from ._lib import FaError, fa_bwd, fa_fwd, fa_fwd_fp8
+from ._lib import FaError, fa_bwd, fa_fp8_quantize, fa_fwd, fa_fwd_fp8
 
 
 def _check(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int, device) -> None:
@@ -252,3 +252,70 @@ def fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, vt8: torch.Tensor, q_descale: to
     if st != 0:
         raise FaError(st, "fa_fwd_fp8")
     return out, lse
+
+
+def hadamard_signs(d: int, seed: int, device=None) -> torch.Tensor:
+    """A seeded vector of d random signs (+1 / -1, int8) for ``fp8_quantize``.
+
+    Rotate Q and K of one problem with the same vector, so that Q K^T is
+    unchanged; the draw is torch's CPU generator, copied to ``device``.
+    """
+    g = torch.Generator().manual_seed(int(seed))
+    s = torch.randint(0, 2, (int(d),), generator=g, dtype=torch.int8) * 2 - 1
+    return s.to(device) if device is not None else s
+
+
+def fp8_quantize(x: torch.Tensor, signs: Optional[torch.Tensor] = None, transpose: bool = False,
+                 out: Optional[torch.Tensor] = None, descale: Optional[torch.Tensor] = None,
+                 stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """e4m3 codes of a bf16 tensor with one descale per (batch, head); returns (x8, descale).
+
+    x [B, H, N, d] bf16 on the GPU (d = 64 or 128).  x8 is uint8 [B, H, N, d],
+    or [B, H, d, N] with ``transpose`` (the layout ``fwd_fp8`` takes for V;
+    N a multiple of 16).  With ``signs`` (int8 [d] of +-1 on the same device,
+    see ``hadamard_signs``) each row is rotated by diag(signs) H_d / sqrt(d)
+    first: the incoherent processing of the 8-bit path.  code * descale[b, h]
+    approximates the (rotated) value.
+    """
+    _check(x, "x", torch.bfloat16, 4, None)
+    dev = x.device
+    B, H, N, d = x.shape
+    shape = (B, H, d, N) if transpose else (B, H, N, d)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.uint8, device=dev)
+    else:
+        _check(out, "out", torch.uint8, 4, dev)
+        if tuple(out.shape) != shape:
+            raise ValueError("out must be %s" % (shape,))
+    if descale is None:
+        descale = torch.empty((B, H), dtype=torch.float32, device=dev)
+    else:
+        _check(descale, "descale", torch.float32, 2, dev)
+        if tuple(descale.shape) != (B, H):
+            raise ValueError("descale must be %s" % ((B, H),))
+    sp = 0
+    if signs is not None:
+        _check(signs, "signs", torch.int8, 1, dev)
+        if signs.numel() != d:
+            raise ValueError("signs must have d = %d entries" % d)
+        sp = signs.data_ptr()
+    with torch.cuda.device(dev):
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        st = fa_fp8_quantize(x.data_ptr(), out.data_ptr(), descale.data_ptr(), B, H, N, d, bool(transpose),
+                             sp or None, s.cuda_stream)
+    if st != 0:
+        raise FaError(st, "fa_fp8_quantize")
+    return out, descale
+
+
+def fwd_fp8_from_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                      scale: Optional[float] = None, rotate: bool = True, seed: int = 0,
+                      stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The 8-bit forward from bf16 inputs: quantizes Q and K (rotated with one
+    seeded sign vector when ``rotate``) and V (transposed), then runs
+    ``fwd_fp8``; returns (O bf16, LSE fp32).  d must be 128."""
+    signs = hadamard_signs(q.shape[-1], seed, q.device) if rotate else None
+    q8, qd = fp8_quantize(q, signs, stream=stream)
+    k8, kd = fp8_quantize(k, signs, stream=stream)
+    vt8, vd = fp8_quantize(v, None, transpose=True, stream=stream)
+    return fwd_fp8(q8, k8, vt8, qd, kd, vd, causal=causal, scale=scale, stream=stream)

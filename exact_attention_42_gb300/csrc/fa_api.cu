@@ -149,6 +149,28 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
                             stream, env);
 }
 
+fa_status fa_fp8_quantize(const void* x, void* x8, float* descale, int B, int H, int N, int d, int transpose,
+                          const int8_t* signs, cudaStream_t stream) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (transpose && N % 16 != 0) return FA_ERR_SHAPE;  // rows of the transpose are N bytes
+  if (B == 0 || H == 0) return FA_OK;
+  if (static_cast<long long>(B) * H > 0x7fffffffLL) return FA_ERR_SHAPE;
+  if (descale == nullptr) return FA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(descale) & 3u) != 0) return FA_ERR_ALIGN;
+  const long long blocks = static_cast<long long>(B) * H * ((N + 63) / 64);
+  if (blocks > 0x7fffffffLL) return FA_ERR_SHAPE;
+  if (N > 0) {
+    if (x == nullptr || x8 == nullptr) return FA_ERR_NULL;
+    auto mis16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) != 0; };
+    if (mis16(x) || mis16(x8)) return FA_ERR_ALIGN;
+  }
+  fa::LaunchEnv env;
+  const fa_status st = fa::launch_env(&env);
+  if (st != FA_OK) return st;
+  return fa::launch_fp8_quantize(x, x8, descale, B, H, N, d, transpose, signs, stream);
+}
+
 int fa_bwd_smem_bytes(int d) { return fa::bwd_smem_bytes(d); }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,

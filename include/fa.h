@@ -152,6 +152,37 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
                      int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
                      cudaStream_t stream);
 
+/*
+ * fa_fp8_quantize -- e4m3 codes and per-(batch, head) descales of one bf16
+ * tensor, for fa_fwd_fp8, on `stream`.  The FA3 canvas ("FlashAttention v3
+ * Hopper asynchrony", element pseudo-code) names block scaling of Q, K and V
+ * and incoherent processing as what keeps the 8-bit path accurate.  Here a
+ * block is one (batch, head) slice, and the incoherent processing is the
+ * optional rotation below.
+ *   x       [B, H, N, d] bf16 (device, 16-byte aligned), d = 64 or 128
+ *   x8      [B, H, N, d] e4m3 codes, or [B, H, d, N] when transpose != 0
+ *           (the layout fa_fwd_fp8 takes for V); device, 16-byte aligned
+ *   descale [B, H] fp32 (device, 4-byte aligned)
+ *   signs   [d] int8, each +1 or -1 (device), or NULL for no rotation
+ * With signs, every row is first multiplied by M = diag(signs) H_d / sqrt(d),
+ * H_d the Sylvester-Hadamard matrix: M is orthogonal, so Q and K rotated with
+ * the same signs give the same Q K^T, while a large channel is spread over
+ * all d before rounding.  V is not rotated.  Per slice, with y the rotated
+ * (unnormalised, (x * signs) H_d) or plain row values and a = max |y|:
+ *   code = e4m3(y * (448 / a)) (nearest even, saturating; 0 when a = 0),
+ *   descale = a / (448 sqrt(d)) with rotation, a / 448 without,
+ * so that code * descale approximates x M (or x).  The values are computed in
+ * float32 with the Walsh-Hadamard butterflies (strides 1, 2, ..., d/2), so the
+ * codes do not depend on launch order.
+ * Errors: FA_ERR_SHAPE for negative sizes or, with transpose, N not a
+ * multiple of 16; FA_ERR_UNSUPPORTED for other d; FA_ERR_NULL / FA_ERR_ALIGN
+ * as described; an empty tensor returns FA_OK.  Three kernels are enqueued;
+ * descale doubles as the slice-maximum accumulator between them, and no
+ * other memory is used.  Argument errors leave the outputs untouched.
+ */
+fa_status fa_fp8_quantize(const void* x, void* x8, float* descale, int B, int H, int N, int d, int transpose,
+                          const int8_t* signs, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* fa_status_string(fa_status s);
 
