@@ -37,6 +37,10 @@ namespace quant {
 constexpr int ROWS_PER_BLOCK = 64;
 constexpr int THREADS = 128;  // four warps of 16 rows each
 constexpr int ROWS_PER_WARP = ROWS_PER_BLOCK / (THREADS / 32);
+// Rows a warp loads before using any of them: one 256-byte row in flight per
+// warp left the kernels at about a third of the HBM bandwidth.
+constexpr int BATCH = 8;
+static_assert(ROWS_PER_WARP % BATCH == 0, "a warp's rows come in whole batches");
 
 // Lane l holds columns [l * E, l * E + E) of a row, E = D / 32.
 template <int D>
@@ -113,12 +117,23 @@ __global__ void __launch_bounds__(THREADS) amax_kernel(const Args a) {
   float sg[D / 32];
   if (a.signs != nullptr) load_signs<D>(a.signs, lane, sg);
   float m = 0.f;
-  for (int r = r0; r < min(r0 + ROWS_PER_WARP, a.N); ++r) {
-    float v[D / 32];
-    load_row<D>(a.x + (static_cast<long long>(slice) * a.N + r) * D, lane, v);
-    if (a.signs != nullptr) rotate_row<D>(v, sg, lane);
+  for (int rb = r0; rb < min(r0 + ROWS_PER_WARP, a.N); rb += BATCH) {
+    float v[BATCH][D / 32];
 #pragma unroll
-    for (int i = 0; i < D / 32; ++i) m = fmaxf(m, fabsf(v[i]));
+    for (int b = 0; b < BATCH; ++b) {
+      if (rb + b < a.N) {
+        load_row<D>(a.x + (static_cast<long long>(slice) * a.N + rb + b) * D, lane, v[b]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) v[b][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+      if (a.signs != nullptr) rotate_row<D>(v[b], sg, lane);
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) m = fmaxf(m, fabsf(v[b][i]));
+    }
   }
   // Non-negative floats order like their bit patterns.
   const uint32_t bits = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
@@ -138,23 +153,37 @@ __global__ void __launch_bounds__(THREADS) quant_kernel(const Args a) {
   if (a.signs != nullptr) load_signs<D>(a.signs, lane, sg);
   const float amax = __uint_as_float(__ldg(reinterpret_cast<const unsigned int*>(a.descale) + slice));
   const float inv = amax > 0.f ? __fdiv_rn(448.f, amax) : 0.f;
-  for (int r = r0; r < min(r0 + ROWS_PER_WARP, a.N); ++r) {
-    float v[E];
-    load_row<D>(a.x + (static_cast<long long>(slice) * a.N + r) * D, lane, v);
-    if (a.signs != nullptr) rotate_row<D>(v, sg, lane);
-    uint32_t packed = 0u;  // E codes, column lane * E first
+  for (int rb = r0; rb < min(r0 + ROWS_PER_WARP, a.N); rb += BATCH) {
+    float v[BATCH][E];
 #pragma unroll
-    for (int i = 0; i < E; i += 2) packed |= e4m3x2(__fmul_rn(v[i], inv), __fmul_rn(v[i + 1], inv)) << (8 * i);
-    if constexpr (TRANSPOSE) {
-      uint8_t* dst = tile + (r - tile_r0) * PITCH + lane * E;
+    for (int b = 0; b < BATCH; ++b) {
+      if (rb + b < a.N) {
+        load_row<D>(a.x + (static_cast<long long>(slice) * a.N + rb + b) * D, lane, v[b]);
+      } else {
 #pragma unroll
-      for (int i = 0; i < E; ++i) dst[i] = static_cast<uint8_t>(packed >> (8 * i));
-    } else {
-      uint8_t* dst = a.x8 + (static_cast<long long>(slice) * a.N + r) * D + lane * E;
-      if constexpr (E == 4)
-        *reinterpret_cast<uint32_t*>(dst) = packed;
-      else
-        *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
+        for (int i = 0; i < E; ++i) v[b][i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < BATCH; ++b) {
+      const int r = rb + b;
+      if (a.signs != nullptr) rotate_row<D>(v[b], sg, lane);  // every lane takes part in the shuffles
+      if (r >= a.N) continue;
+      uint32_t packed = 0u;  // E codes, column lane * E first
+#pragma unroll
+      for (int i = 0; i < E; i += 2)
+        packed |= e4m3x2(__fmul_rn(v[b][i], inv), __fmul_rn(v[b][i + 1], inv)) << (8 * i);
+      if constexpr (TRANSPOSE) {
+        uint8_t* dst = tile + (r - tile_r0) * PITCH + lane * E;
+#pragma unroll
+        for (int i = 0; i < E; ++i) dst[i] = static_cast<uint8_t>(packed >> (8 * i));
+      } else {
+        uint8_t* dst = a.x8 + (static_cast<long long>(slice) * a.N + r) * D + lane * E;
+        if constexpr (E == 4)
+          *reinterpret_cast<uint32_t*>(dst) = packed;
+        else
+          *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
+      }
     }
   }
   if constexpr (TRANSPOSE) {
