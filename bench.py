@@ -121,8 +121,80 @@ def load_traffic(workload: str, kernel: str = "fa_fwd_kernel"):
     return e.get("dram_bytes_per_launch")
 
 
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read through NVML (read-only
+    queries) every millisecond on a background thread, so that even a timed
+    region of a few milliseconds has samples.  mark_start / mark_stop bracket
+    the timed region; stop() summarises the samples taken inside it."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str):
+        import ctypes
+        import threading
+        self.ct = ctypes
+        self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.nvml.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        if self.nvml.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.handle)) != 0:
+            raise OSError("no NVML device with uuid %s" % uuid)
+        self.get_reasons = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        self.sm_max = float(mx.value)
+        self.samples = []
+        self.window = [None, None]
+        self.stop_evt = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _read(self):
+        ct = self.ct
+        clk, mw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(clk))
+        self.nvml.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw))
+        self.get_reasons(self.handle, ct.byref(rs))
+        return time.perf_counter(), float(clk.value), mw.value / 1000.0, int(rs.value)
+
+    def _run(self):
+        while not self.stop_evt.is_set():
+            self.samples.append(self._read())
+            time.sleep(0.001)
+
+    def start(self):
+        self.thread.start()
+
+    def mark_start(self):
+        self.samples.append(self._read())
+        self.window[0] = time.perf_counter()
+
+    def mark_stop(self):
+        self.window[1] = time.perf_counter()
+        self.samples.append(self._read())
+
+    def stop(self):
+        self.stop_evt.set()
+        self.thread.join(timeout=5)
+        try:
+            self.nvml.nvmlShutdown()
+        except Exception:
+            pass
+        t0, t1 = self.window
+        inside = [x for x in self.samples if t0 is not None and t1 is not None and t0 <= x[0] <= t1]
+        use = inside or self.samples
+        if not use:
+            return None
+        reasons = sorted({name for x in use for bit, name in self.REASONS.items() if x[3] & bit})
+        return {"sm_mhz": statistics.median(x[1] for x in use), "sm_max_mhz": self.sm_max, "reasons": reasons,
+                "samples": len(use), "samples_in_timed_region": len(inside),
+                "power_w_median": statistics.median(x[2] for x in use),
+                "source": "NVML, 1 ms polling during the timed region"}
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples every 200 ms."""
+    """nvidia-smi clock / throttle-reason samples every 200 ms (used when NVML
+    cannot be loaded)."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -171,7 +243,39 @@ class ClockSampler:
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons,
                 "samples": len(rows), "power_w_median": statistics.median(
-                    [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()] or [0.0])}
+                    [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()] or [0.0]),
+                "source": "nvidia-smi -lms 200 over warm-up and timed region"}
+
+    def mark_start(self):
+        pass
+
+    def mark_stop(self):
+        pass
+
+
+def host_cpu():
+    """Logical CPUs of the host and its model name (for the CPU baseline)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if model is None:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    import platform
+    return {"nproc": os.cpu_count(), "model": model or platform.processor() or platform.machine()}
 
 
 def dist_setup():
@@ -206,12 +310,26 @@ def is_decode(prob) -> bool:
     return (not prob.varlen) and prob.Nk > 0 and (prob.Hq // prob.Hkv) * prob.Nq <= 16
 
 
-def workload_config(prob, name):
+def step_bytes(prob, bwd: bool = False, fp8: bool = False) -> int:
+    """Bytes of one input set and its outputs (what one timed step touches)."""
+    rows = prob.q.size // prob.d
+    qkv = (prob.q.size + prob.k.size + prob.v.size) * (1 if fp8 else 2)
+    out = 2 * prob.q.size + 4 * rows                      # O bf16, LSE fp32
+    if bwd:
+        # O, LSE and dO in; dQ, dK, dV and delta out.
+        return qkv + out + 2 * prob.q.size + 2 * (prob.q.size + prob.k.size + prob.v.size) + 4 * rows
+    return qkv + out
+
+
+def workload_config(prob, name, world: int = 1, bwd: bool = False, fp8: bool = False):
     cfg = {"workload": name, "B": prob.B, "Hq": prob.Hq, "Hkv": prob.Hkv, "Nq": prob.Nq, "Nk": prob.Nk,
            "d": prob.d, "causal": prob.causal, "flop_per_step": prob.flops()}
     if prob.varlen:
         cfg["seqlens"] = prob.seqlens()
         cfg["total_tokens"] = int(prob.cu_seqlens[-1])
+    cfg["parallelism"] = "replicas" if world > 1 else "single"
+    cfg["l2"] = "inputs rotated over %d copies (%.0f MB > %d MB L2)" % (
+        ROTATE, ROTATE * step_bytes(prob, bwd, fp8) / 1e6, L2_BYTES // 2 ** 20)
     return cfg
 
 
@@ -295,9 +413,9 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": workload_config(prob, name),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": "per step: " + descs[-1]},
+            "config": workload_config(prob, name, args.gpus, args.bwd, args.fp8),
+            "cpu_baseline": dict({"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                  "sample": "per step: " + descs[-1]}, **host_cpu()),
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line))
@@ -359,7 +477,6 @@ def run_ours(args):
             sets.append((q, k, v, o, lse, do) + grads)
         else:
             sets.append((q, k, v, o, lse))
-    step_bytes = sum(t.numel() * t.element_size() for t in sets[0])
     stream = torch.cuda.current_stream(dev)
     launches_per_step = 3 if args.bwd else 1
 
@@ -383,7 +500,10 @@ def run_ours(args):
             gid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
         except Exception:
             gid = None
-        sampler = ClockSampler(gid)
+        try:
+            sampler = NvmlClockSampler(gid)
+        except (OSError, AttributeError, TypeError):
+            sampler = ClockSampler(gid)
         sampler.start()
     for i in range(args.warmup):
         step(i)
@@ -391,17 +511,35 @@ def run_ours(args):
     barrier(world, dev)
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.mark_start()
     ev0.record(stream)
     for i in range(args.steps):
         step(i)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark_stop()
     barrier(world, dev)
     clocks = sampler.stop() if sampler else None
     ms_total = ev0.elapsed_time(ev1)
     ms_step = reduce_max(ms_total / args.steps, world, dev)
     status_bits = fa.fa_device_status()
     value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # Warm-L2 figure, for context beside the cold one above: the same input
+    # set every step (whatever of it fits stays in L2).  Not the bench value.
+    warm_steps = max(3, min(args.steps, 50))
+    for _ in range(3):
+        step(0)
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
+    for _ in range(warm_steps):
+        step(0)
+    w1.record(stream)
+    torch.cuda.synchronize(dev)
+    warm_ms = w0.elapsed_time(w1) / warm_steps
+    status_bits |= fa.fa_device_status()
 
     # End to end through the public API: pinned host inputs copied in, the
     # kernels, the results copied back, every step.
@@ -506,10 +644,10 @@ def run_ours(args):
             "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3" if args.fp8 else "bf16", "data": "synthetic",
-            "config": dict(workload_config(prob, name), parallelism="replicas" if world > 1 else "single",
-                           l2="inputs rotated over %d copies (%.0f MB > %d MB L2)"
-                              % (ROTATE, ROTATE * step_bytes / 1e6, L2_BYTES // 2 ** 20)),
+            "config": workload_config(prob, name, world, args.bwd, args.fp8),
             "roofline": roofline,
+            "warm_l2": {"ms_per_step": warm_ms, "value": flops / (warm_ms * 1e-3) / 1e12, "unit": UNIT,
+                        "steps": warm_steps, "note": "one input set reused every step; context only"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "call": "fwd_host" if host_api else "copies + " + ("bwd" if args.bwd else "fwd_fp8"),
                     "ms_per_step": e2e_ms},
@@ -519,7 +657,8 @@ def run_ours(args):
             "kernel_sha": kernel_hash(roofline["kernel"])}
     if rank == 0 and not args.no_cpu_baseline:
         v_cpu, threads, desc, _ = oracle_sample(prob, args.cpu_budget_s, backward=args.bwd)
-        line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc}
+        line["cpu_baseline"] = dict({"value": v_cpu, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                     "sample": desc}, **host_cpu())
     if rank == 0:
         print(json.dumps(line))
     if world > 1:

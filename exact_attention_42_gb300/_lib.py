@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_threads.restype = ci
             L.fa_debug_fault_injection.argtypes = [ci, ctypes.c_double]
             L.fa_debug_fault_injection.restype = ci
+            L.fa_debug_soft_exp.argtypes = [ci]
+            L.fa_debug_soft_exp.restype = ci
             L.fa_debug_exp2_soft.argtypes = [vp, vp, ci, vp]
             L.fa_debug_exp2_soft.restype = ci
             L.fa_decode.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, ci, vp]
@@ -104,7 +106,7 @@ def fa_status_string(status: int) -> str:
 
 
 def fa_device_status() -> int:
-    """Reads and clears the device status word (synchronises the device)."""
+    """Reads and clears the device status words (waits for all work on the device first)."""
     bits = ctypes.c_int(0)
     st = lib().fa_device_status(ctypes.byref(bits))
     if st not in (0, 6):
@@ -113,10 +115,17 @@ def fa_device_status() -> int:
 
 
 def fa_debug_fault_injection(mode: int, wait_limit_seconds: float = 0.0) -> None:
-    """Test hook: mode 1 makes later launches time out on purpose (see fa.h)."""
+    """Test hook: modes 1-4 make one kernel's later launches time out on purpose (see fa.h)."""
     st = lib().fa_debug_fault_injection(int(mode), float(wait_limit_seconds))
     if st != 0:
         raise FaError(st, "fa_debug_fault_injection")
+
+
+def fa_debug_soft_exp(on: int) -> None:
+    """Test hook: 1 selects the forward kernels with software exponentials (see fa.h)."""
+    st = lib().fa_debug_soft_exp(int(on))
+    if st != 0:
+        raise FaError(st, "fa_debug_soft_exp")
 
 
 def fa_debug_exp2_soft(x_ptr: int, y_ptr: int, n: int, stream: int = 0) -> None:

@@ -20,9 +20,11 @@ struct DeviceInfo {
   int sms = 0;
 };
 
-// Test hook state (process-wide): see fa_debug_fault_injection.
+// Test hook state (process-wide): see fa_debug_fault_injection and
+// fa_debug_soft_exp.
 static std::atomic<int> g_fault_mode{0};
 static std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+static std::atomic<int> g_soft_exp{0};
 
 static DeviceInfo g_dev[kMaxDevicesDecode];
 static std::mutex g_dev_mutex;
@@ -49,6 +51,7 @@ static fa_status launch_env(LaunchEnv* env) {
   env->sms = di.sms;
   env->wait_limit_ns = g_wait_limit_ns.load();
   env->fault_mode = g_fault_mode.load();
+  env->soft_exp = g_soft_exp.load();
   return FA_OK;
 }
 
@@ -94,6 +97,10 @@ const char* fa_status_string(fa_status s) {
 
 fa_status fa_device_status(int* bits) {
   if (bits == nullptr) return FA_ERR_NULL;
+  // Every stream of the device must be idle first: the word reads and clears
+  // below go through the legacy stream, which does not wait for non-blocking
+  // streams, and a kernel still running there could set a bit between them.
+  if (cudaDeviceSynchronize() != cudaSuccess) return FA_ERR_CUDA;
   int v = fa::fwd_status_and_clear();
   if (v < 0) return FA_ERR_CUDA;
   const int dv = fa::decode_status_and_clear();
@@ -121,7 +128,7 @@ fa_status fa_decode(const void* q, const void* k, const void* v, void* o, float*
   const fa_status st = fa::launch_env(&env);
   if (st != FA_OK) return st;
   return fa::launch_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream, env.sms,
-                           env.wait_limit_ns);
+                           env.wait_limit_ns, env.fault_mode);
 }
 
 int fa_decode_smem_bytes(int d) { return fa::decode_smem_bytes(d); }
@@ -196,17 +203,23 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
   const fa_status st = fa::launch_env(&env);
   if (st != FA_OK) return st;
   return fa::launch_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens,
-                        stream, env.sms, env.wait_limit_ns);
+                        stream, env.sms, env.wait_limit_ns, env.fault_mode);
 }
 
 fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds) {
-  if (mode < 0 || mode > 1) return FA_ERR_VALUE;
+  if (mode < 0 || mode >= fa::kFaultModes) return FA_ERR_VALUE;
   if (!(wait_limit_seconds <= 10.0)) return FA_ERR_VALUE;  // also rejects NaN
   const unsigned long long ns = wait_limit_seconds > 0.0
                                     ? static_cast<unsigned long long>(wait_limit_seconds * 1e9)
                                     : fa::kDefaultWaitLimitNs;
   fa::g_wait_limit_ns.store(ns);
   fa::g_fault_mode.store(mode);
+  return FA_OK;
+}
+
+fa_status fa_debug_soft_exp(int on) {
+  if (on != 0 && on != 1) return FA_ERR_VALUE;
+  fa::g_soft_exp.store(on);
   return FA_OK;
 }
 

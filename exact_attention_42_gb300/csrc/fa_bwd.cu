@@ -42,6 +42,7 @@
 #include <cstdint>
 #include <cstring>
 #include <cmath>
+#include <mutex>
 
 #include "fa.h"
 #include "fa_internal.h"
@@ -130,6 +131,7 @@ struct Params {
   int num_units;     // dense: units of the launched kernel; packed: computed on the device
   const int* cu_seqlens;  // null: dense; else B+1 offsets of packed sequences (Nq == Nk == T)
   unsigned long long wait_limit_ns;
+  int fault_inject;       // test hook: 1 = the launched kernel's ring producer withholds its first fill
 };
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int role) {
@@ -399,6 +401,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int s = it % C::NS;
             if (!(ok = wait_or_abort(empty_bar(s), ((it / C::NS) & 1u) ^ 1u, abort_flag, 0, p.wait_limit_ns)))
               break;
+            if (p.fault_inject && it == 0) {  // test hook: this fill never arrives
+              ++it;
+              continue;
+            }
             mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
             const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
             for (int c = 0; c < C::CHUNKS; ++c)
@@ -788,6 +794,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const int s = it % C::NS;
               if (!(ok = wait_or_abort(empty_bar(s), ((it / C::NS) & 1u) ^ 1u, abort_flag, 4, p.wait_limit_ns)))
                 break;
+              if (p.fault_inject && it == 0) {  // test hook: this fill never arrives
+                ++it;
+                continue;
+              }
               mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
               const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
               for (int c = 0; c < C::CHUNKS; ++c)
@@ -1102,23 +1112,27 @@ template <int D>
 static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv,
                               int Nq, int Nk, float scale, int causal, const int32_t* cu_seqlens,
-                              cudaStream_t stream, int sms, unsigned long long wait_limit_ns) {
+                              cudaStream_t stream, int sms, unsigned long long wait_limit_ns, int fault_mode) {
   const bool packed = cu_seqlens != nullptr;
   // Tensor-map heads: (batch, head) pairs, or heads alone when packed.
   const long long q_heads = packed ? Hq : static_cast<long long>(B) * Hq;
   const long long kv_heads = packed ? Hkv : static_cast<long long>(B) * Hkv;
   using CQ = bwd::Cfg<D, false>;
   using CKV = bwd::Cfg<D, true>;
-  static bool attr_set[kMaxDevicesDecode] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  if (dev >= 0 && dev < kMaxDevicesDecode && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(bwd::bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CQ::SMEM_BYTES) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(bwd::bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             CKV::SMEM_BYTES) != cudaSuccess)
-      return FA_ERR_CUDA;
-    attr_set[dev] = true;
+  {
+    static std::mutex mu;
+    static bool attr_set[kMaxDevicesDecode] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevicesDecode && !attr_set[dev]) {
+      if (cudaFuncSetAttribute(bwd::bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, CQ::SMEM_BYTES) !=
+              cudaSuccess ||
+          cudaFuncSetAttribute(bwd::bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               CKV::SMEM_BYTES) != cudaSuccess)
+        return FA_ERR_CUDA;
+      attr_set[dev] = true;
+    }
   }
   // D = rowsum(dO * O) first: both main kernels read it.
   const long long rows = q_heads * Nq;
@@ -1169,6 +1183,7 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
     const long long units = packed ? Hq * tiles_bound : static_cast<long long>(B) * Hq * prm.nqt;
     if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
     prm.num_units = packed ? -1 : static_cast<int>(units);
+    prm.fault_inject = fault_mode == kFaultBwdDq ? 1 : 0;
     const long long grid = units < sms ? units : sms;
     if (grid > 0) {
       bwd::bwd_dq_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, CQ::SMEM_BYTES, stream>>>(tq, tdo, tk,
@@ -1181,6 +1196,7 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
     const long long units = packed ? Hkv * tiles_bound : static_cast<long long>(B) * Hkv * prm.nkt;
     if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
     prm.num_units = packed ? -1 : static_cast<int>(units);
+    prm.fault_inject = fault_mode == kFaultBwdDkdv ? 1 : 0;
     const long long grid = units < sms ? units : sms;
     if (grid > 0) {
       bwd::bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, CKV::SMEM_BYTES, stream>>>(
@@ -1194,12 +1210,12 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
 fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                      void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int Nq, int Nk, int d,
                      float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream, int sms,
-                     unsigned long long wait_limit_ns) {
+                     unsigned long long wait_limit_ns, int fault_mode) {
   if (d == 128)
     return launch_bwd_t<128>(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens,
-                             stream, sms, wait_limit_ns);
+                             stream, sms, wait_limit_ns, fault_mode);
   return launch_bwd_t<64>(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens,
-                          stream, sms, wait_limit_ns);
+                          stream, sms, wait_limit_ns, fault_mode);
 }
 
 }  // namespace fa

@@ -35,6 +35,7 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 #include <cmath>
+#include <mutex>
 
 #include "fa.h"
 #include "fa_internal.h"
@@ -75,6 +76,7 @@ struct Params {
   int causal;
   int keys_per_split;  // multiple of BLOCK_N
   unsigned long long wait_limit_ns;
+  int fault_inject;    // test hook: 1 = every producer withholds its first tile
 };
 
 __device__ int g_decode_status;
@@ -184,6 +186,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       int issued = 0;
+      int withheld = -1;
       for (int t = 0; t < ntiles; ++t) {
         const int s = t % STAGES;
         if (t >= STAGES &&
@@ -193,6 +196,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             atomicOr(&g_decode_status, 1);
           }
           break;
+        }
+        if (p.fault_inject && t == 0) {  // test hook: this tile never arrives
+          withheld = t;
+          issued = t + 1;
+          continue;
         }
         const uint32_t bar = smem_u32(&full[s]);
         mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
@@ -211,7 +219,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         __shared__ int never;
         never = 0;
         for (int t = max(0, issued - STAGES); t < issued; ++t)
-          mbar_wait(smem_u32(&full[t % STAGES]), (t / STAGES) & 1u, &never, p.wait_limit_ns);
+          if (t != withheld) mbar_wait(smem_u32(&full[t % STAGES]), (t / STAGES) & 1u, &never, p.wait_limit_ns);
       }
     }
     __syncwarp();
@@ -436,15 +444,19 @@ bool decode_supported(int B, int Hq, int Hkv, int Nq, int Nk, int d, const int32
 template <int D>
 static fa_status launch_decode_t(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                                  int Hkv, int Nq, int Nk, float scale, int causal, cudaStream_t stream, int sms,
-                                 unsigned long long wait_limit_ns) {
-  static bool attr_set[kMaxDevicesDecode] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  if (dev >= 0 && dev < kMaxDevicesDecode && !attr_set[dev]) {
-    if (cudaFuncSetAttribute(dec::decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             dec::Cfg<D>::SMEM_BYTES) != cudaSuccess)
-      return FA_ERR_CUDA;
-    attr_set[dev] = true;
+                                 unsigned long long wait_limit_ns, int fault_mode) {
+  {
+    static std::mutex mu;
+    static bool attr_set[kMaxDevicesDecode] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev >= 0 && dev < kMaxDevicesDecode && !attr_set[dev]) {
+      if (cudaFuncSetAttribute(dec::decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               dec::Cfg<D>::SMEM_BYTES) != cudaSuccess)
+        return FA_ERR_CUDA;
+      attr_set[dev] = true;
+    }
   }
   alignas(64) CUtensorMap tk, tv;
   if (!encode_decode_map(&tk, k, D, Nk, static_cast<long long>(B) * Hkv) ||
@@ -477,6 +489,7 @@ static fa_status launch_decode_t(const void* q, const void* k, const void* v, vo
   prm.causal = causal ? 1 : 0;
   prm.keys_per_split = static_cast<int>(kps);
   prm.wait_limit_ns = wait_limit_ns;
+  prm.fault_inject = fault_mode == kFaultDecode ? 1 : 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(groups), 1);
@@ -496,10 +509,12 @@ static fa_status launch_decode_t(const void* q, const void* k, const void* v, vo
 
 fa_status launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                         int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream, int sms,
-                        unsigned long long wait_limit_ns) {
+                        unsigned long long wait_limit_ns, int fault_mode) {
   if (d == 128)
-    return launch_decode_t<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, sms, wait_limit_ns);
-  return launch_decode_t<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, sms, wait_limit_ns);
+    return launch_decode_t<128>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, sms, wait_limit_ns,
+                                fault_mode);
+  return launch_decode_t<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, stream, sms, wait_limit_ns,
+                             fault_mode);
 }
 
 int decode_status_and_clear() {

@@ -103,24 +103,18 @@ constexpr int PREFETCH_KV_TILES = 3;
 #endif
 constexpr int P_PARTS = FA_P_PARTS;
 static_assert(P_PARTS == 1 || P_PARTS == 2 || P_PARTS == 4, "P_PARTS divides the four 32-key chunks");
-// Software exponentials: in tiles without a mask, one score pair in every
-// SOFT_EXP_PERIOD is exponentiated on the FMA/ALU pipes (exp2_soft2) instead
-// of the MUFU unit; 0 turns this off.  Off by default: on GB300 the MUFU unit
-// runs at about a quarter of its peak in this kernel while the softmax warps
-// are bound by instruction issue, and moving one pair in 4 (3, 2) to the
-// polynomial made the B2/H32/N4096/d128 causal forward 24% (29%, 41%) slower.
-#ifndef FA_SOFT_EXP_PERIOD
-#define FA_SOFT_EXP_PERIOD 0
-#endif
-constexpr int SOFT_EXP_PERIOD = FA_SOFT_EXP_PERIOD;
-// The same for the 8-bit path, whose products take half the tensor time, so
-// that its softmax is more often the limit.  Off as well: on GB300 one pair in
-// 4 (3, 2) made the B2/H32/N4096 causal 8-bit forward 24% (30%, 40%) slower;
-// its softmax warps are bound by instruction issue, not by the MUFU unit.
-#ifndef FA_SOFT_EXP_PERIOD_FP8
-#define FA_SOFT_EXP_PERIOD_FP8 0
-#endif
-constexpr int SOFT_EXP_PERIOD_FP8 = FA_SOFT_EXP_PERIOD_FP8;
+// Software exponentials: the kernel's SOFT template argument, when non-zero,
+// sends one score pair in every SOFT of a tile without a mask through
+// exp2_soft2 (FMA/ALU pipes) instead of the MUFU unit.  The library launches
+// SOFT = 0 unless fa_debug_soft_exp selects the SOFT_EXP_PERIOD instantiation.
+// It stays off by default: on GB300 the MUFU unit runs at about a quarter of
+// its peak in this kernel while the softmax warps are bound by instruction
+// issue, and moving one pair in 4 (3, 2) to the polynomial made the
+// B2/H32/N4096/d128 causal forward 24% (29%, 41%) slower, and the 8-bit
+// forward 24% (30%, 40%) slower.  The instantiation kept is the one that
+// sends the most exponentials through the polynomial (one pair in 2), so that
+// the parity tests cover it as fully as possible.
+constexpr int SOFT_EXP_PERIOD = 2;
 
 // Device status word: bit (1 << role) is set when that role gave up waiting.
 __device__ int g_fa_status;
@@ -310,7 +304,7 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, volati
   if (!mbar_wait(bar, parity, &never, limit_ns)) raise_abort(abort_flag, role);
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, int SOFT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -718,8 +712,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int i = 0; i < 16; ++i) {
               const float2 x = fma2(make_float2(s[c0 + 2 * i], s[c0 + 2 * i + 1]), c2, nb2);
               float2 e;
-              constexpr int period = FP8 ? SOFT_EXP_PERIOD_FP8 : SOFT_EXP_PERIOD;
-              if (period > 0 && (i % (period > 0 ? period : 1)) == period - 1 && !need_mask)
+              if (SOFT > 0 && (i % (SOFT > 0 ? SOFT : 1)) == SOFT - 1 && !need_mask)
                 e = exp2_soft2(x);  // no -inf here: the tile has no masked score
               else
                 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
@@ -853,24 +846,33 @@ static bool encode_rows_map(CUtensorMap* map, const void* base, int d, long long
   return encode_bf16_rows_map(map, base, d, rows, heads, BLOCK_M);
 }
 
+// Raises the dynamic shared-memory limit of one kernel instantiation, once
+// per device (the attribute applies to the current device).
+template <int D, bool FP8, int SOFT>
+static bool prepare_kernel(int device) {
+  static std::mutex mu;
+  static bool attr_set[kMaxDevicesDecode] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (device < 0 || device >= kMaxDevicesDecode) return false;
+  if (!attr_set[device]) {
+    if (cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, SOFT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<D, FP8>::SMEM_BYTES) != cudaSuccess)
+      return false;
+    attr_set[device] = true;
+  }
+  return true;
+}
+
 template <int D>
 static fa_status launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                         int Nq, int Nk, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream,
                         const LaunchEnv& env) {
   if (decode_supported(B, Hq, Hkv, Nq, Nk, D, cu_seqlens))
-    return launch_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, stream, env.sms, env.wait_limit_ns);
-  {
-    static std::mutex mu;
-    static bool attr_set[kMaxDevicesDecode] = {};
-    std::lock_guard<std::mutex> lock(mu);
-    if (env.device < 0 || env.device >= kMaxDevicesDecode) return FA_ERR_CUDA;
-    if (!attr_set[env.device]) {
-      if (cudaFuncSetAttribute(fa_fwd_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<D>::SMEM_BYTES) != cudaSuccess)
-        return FA_ERR_CUDA;
-      attr_set[env.device] = true;
-    }
-  }
+    return launch_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, stream, env.sms, env.wait_limit_ns,
+                         env.fault_mode);
+  const bool soft = env.soft_exp != 0;
+  if (!(soft ? prepare_kernel<D, false, SOFT_EXP_PERIOD>(env.device) : prepare_kernel<D, false, 0>(env.device)))
+    return FA_ERR_CUDA;
   const bool packed = cu_seqlens != nullptr;
   alignas(64) CUtensorMap tq, tk, tv;
   std::memset(&tq, 0, sizeof(tq));
@@ -898,7 +900,7 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.causal = causal ? 1 : 0;
   prm.wait_limit_ns = env.wait_limit_ns;
-  prm.fault_inject = env.fault_mode;
+  prm.fault_inject = env.fault_mode == kFaultFwd ? 1 : 0;
   prm.q_descale = prm.k_descale = prm.v_descale = nullptr;
   long long grid;
   if (packed) {
@@ -915,7 +917,11 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
     grid = units < env.sms ? units : env.sms;
   }
   if (grid <= 0) return FA_OK;
-  fa_fwd_kernel<D, false><<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+  if (soft)
+    fa_fwd_kernel<D, false, SOFT_EXP_PERIOD>
+        <<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+  else
+    fa_fwd_kernel<D, false, 0><<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -946,18 +952,9 @@ fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const 
                          int Nq, int Nk, float scale, int causal, cudaStream_t stream, const LaunchEnv& env) {
   constexpr int D = 128;
   using C = Cfg<D, true>;
-  {
-    static std::mutex mu;
-    static bool attr_set[kMaxDevicesDecode] = {};
-    std::lock_guard<std::mutex> lock(mu);
-    if (env.device < 0 || env.device >= kMaxDevicesDecode) return FA_ERR_CUDA;
-    if (!attr_set[env.device]) {
-      if (cudaFuncSetAttribute(fa_fwd_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-          cudaSuccess)
-        return FA_ERR_CUDA;
-      attr_set[env.device] = true;
-    }
-  }
+  const bool soft = env.soft_exp != 0;
+  if (!(soft ? prepare_kernel<D, true, SOFT_EXP_PERIOD>(env.device) : prepare_kernel<D, true, 0>(env.device)))
+    return FA_ERR_CUDA;
   alignas(64) CUtensorMap tq, tk, tv;
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
@@ -988,7 +985,11 @@ fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const 
   prm.num_units = static_cast<int>(units);
   const long long grid = units < env.sms ? units : env.sms;
   if (grid <= 0) return FA_OK;
-  fa_fwd_kernel<D, true><<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+  if (soft)
+    fa_fwd_kernel<D, true, SOFT_EXP_PERIOD><<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM_BYTES, stream>>>(
+        tq, tk, tv, prm);
+  else
+    fa_fwd_kernel<D, true, 0><<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }

@@ -12,12 +12,22 @@ namespace fa {
 constexpr int kMaxDevicesDecode = 64;                      // devices with per-device launch state
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // bound on every kernel wait: 2 s
 
+// Fault-injection modes of fa_debug_fault_injection: which kernel's ring
+// producer withholds its first copy.
+constexpr int kFaultNone = 0;
+constexpr int kFaultFwd = 1;     // fa_fwd_kernel's K/V producer
+constexpr int kFaultDecode = 2;  // decode_kernel's K/V producer
+constexpr int kFaultBwdDq = 3;   // bwd_dq_kernel's K/V producer
+constexpr int kFaultBwdDkdv = 4; // bwd_dkdv_kernel's Q/dO producer
+constexpr int kFaultModes = 5;
+
 // Per-call launch settings resolved by the entry points (fa_api.cu).
 struct LaunchEnv {
   int device = 0;
   int sms = 0;                          // streaming multiprocessors of the device
   unsigned long long wait_limit_ns = 0;  // bound on every mbarrier wait
   int fault_mode = 0;                   // test hook, see fa_debug_fault_injection
+  int soft_exp = 0;                     // test hook, see fa_debug_soft_exp
 };
 
 // Forward kernel (fa_fwd.cu); dispatches to the split-KV path itself.
@@ -45,7 +55,7 @@ bool encode_bf16_rows_map(CUtensorMap* map, const void* base, int d, long long r
 bool decode_supported(int B, int Hq, int Hkv, int Nq, int Nk, int d, const int32_t* cu_seqlens);
 fa_status launch_decode(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                         int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream, int sms,
-                        unsigned long long wait_limit_ns);
+                        unsigned long long wait_limit_ns, int fault_mode);
 int decode_status_and_clear();  // -1 if the status word cannot be read
 int decode_smem_bytes(int d);
 
@@ -53,7 +63,7 @@ int decode_smem_bytes(int d);
 fa_status launch_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                      void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int Nq, int Nk, int d,
                      float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream, int sms,
-                     unsigned long long wait_limit_ns);
+                     unsigned long long wait_limit_ns, int fault_mode);
 int bwd_status_and_clear();  // -1 if the status word cannot be read
 int bwd_smem_bytes(int d);
 

@@ -17,8 +17,12 @@
  *   - grouped-query attention: query head h reads key/value head h / (Hq / Hkv);
  *   - P is rounded to bf16 before the P*V product; all accumulation is fp32.
  *
- * Thread safety: every entry point is reentrant.  The library keeps only
- * once-initialised per-device launch settings and one device status word.
+ * Thread safety: every entry point is reentrant.  The library's state is
+ * once-initialised per-device launch settings, three device status words (one
+ * each for the forward, split-KV and backward kernels, merged by
+ * fa_device_status) and the process-wide settings of the two test hooks
+ * (fa_debug_fault_injection, fa_debug_soft_exp): a hook call changes every
+ * later launch, from any thread.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -179,6 +183,12 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
  * as described; an empty tensor returns FA_OK.  Three kernels are enqueued;
  * descale doubles as the slice-maximum accumulator between them, and no
  * other memory is used.  Argument errors leave the outputs untouched.
+ * Non-finite inputs: a NaN element is left out of its slice's maximum and
+ * gets a NaN code (0x7F or 0xFF); an infinite element makes its slice's
+ * maximum and descale +inf, its own code NaN and every other code of the
+ * slice a zero (0x00, or 0x80 for negative values).  With the rotation a
+ * non-finite element first spreads over its whole row (NaN codes for that
+ * row, and for an infinity the slice's other rows become zeros).
  */
 fa_status fa_fp8_quantize(const void* x, void* x8, float* descale, int B, int H, int N, int d, int transpose,
                           const int8_t* signs, cudaStream_t stream);
@@ -194,19 +204,26 @@ const char* fa_status_string(fa_status s);
  * bit 8: the split-KV kernel; bits 9-11 and 13-15: producer, MMA issuer and
  * softmax roles of fa_bwd's dQ and dK/dV kernels.  Returns FA_OK and stores
  * 0 in *bits when nothing went wrong, FA_ERR_TIMEOUT with the bits otherwise.
- * This call synchronises the device (it reads device memory).
+ * The call first waits for all work on the current device (every stream,
+ * cudaDeviceSynchronize), so no kernel can set a bit between the read and the
+ * clear; FA_ERR_CUDA if that or a read fails.
  */
 fa_status fa_device_status(int* bits);
 
 /*
  * fa_debug_fault_injection -- test hook for the failure path (process-wide,
- * affects later fa_fwd calls).  mode 0 is normal operation; mode 1 makes the
- * kernel's K/V producer withhold its first copy, so the bounded waits of the
- * other roles run out: the kernel then records FA_ERR_TIMEOUT bits in the
- * device status word, waits for its own copies in flight, frees its Tensor
- * Memory and exits, leaving the CUDA context usable.  wait_limit_seconds
- * (0 < x <= 10) sets the bound on every wait inside the kernel; 0 restores the
- * default of 2 s.  Returns FA_ERR_VALUE for other arguments.
+ * affects every later launch).  mode 0 is normal operation.  Modes 1-4 make
+ * one kernel's ring producer withhold its first copy, so that the bounded
+ * waits of the roles that need it run out:
+ *   1  fa_fwd's kernel (its K/V producer; status bits 0-4),
+ *   2  the split-KV kernel of fa_decode and fa_fwd (status bit 8),
+ *   3  fa_bwd's dQ kernel (its K/V producer; bits 9-11),
+ *   4  fa_bwd's dK/dV kernel (its Q/dO producer; bits 13-15).
+ * The kernel then records the bits in its device status word, waits (bounded)
+ * for its own copies in flight, frees its Tensor Memory and exits, leaving the
+ * CUDA context usable; its outputs are undefined.  wait_limit_seconds
+ * (0 < x <= 10) sets the bound on every wait inside the kernels; 0 restores
+ * the default of 2 s.  Returns FA_ERR_VALUE for other arguments.
  */
 fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds);
 
@@ -219,6 +236,17 @@ fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds);
  * (The "software exp" of the interview canvas, element v4-card-body.)
  */
 fa_status fa_debug_exp2_soft(const float* x, float* y, int n, cudaStream_t stream);
+
+/*
+ * fa_debug_soft_exp -- test hook (process-wide, affects every later fa_fwd and
+ * fa_fwd_fp8 launch): on = 1 runs the forward kernels' instantiation that
+ * computes one exponential pair in every two of each K/V tile without a mask
+ * with the software 2^x of fa_debug_exp2_soft (FMA/ALU pipes) instead of the
+ * exp unit; on = 0 (the default) restores the normal kernels.  The results
+ * stay within the same tolerances; the path is off by default because it
+ * measured slower on GB300.  FA_ERR_VALUE for other arguments.
+ */
+fa_status fa_debug_soft_exp(int on);
 
 /* Dynamic shared memory (bytes) and threads per CTA used for head dim d;
  * 0 for an unsupported d.  For tooling and tests. */

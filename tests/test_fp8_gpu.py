@@ -19,7 +19,7 @@ import torch
 
 from fa_inputs import make_dense, make_fp8, make_workload
 from fa_testutil import LSE_RTOL
-from oracle import attention_fwd, attention_rows
+from oracle import attention_fwd
 
 pytestmark = pytest.mark.gpu
 
@@ -101,17 +101,20 @@ def test_fp8_is_deterministic(fa, dev):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
 
 
-def test_fp8_headline_sampled(fa, dev):
-    """The B2 H32 N4096 d128 causal workload, quantized, on sampled rows."""
+def test_fp8_headline_full_size(fa, dev):
+    """The B2 H32 N4096 d128 causal workload, quantized: every element of O
+    and LSE against the oracle, one (batch, head) at a time."""
     p = make_workload("b2_h32_n4096_d128_causal")
     f8 = make_fp8(p)
     o, lse = _run(fa, f8, dev)
     q, k, v = f8.dequantized()
-    rng = np.random.default_rng(8)
-    samples = [(int(rng.integers(p.B)), int(rng.integers(p.Hq)), int(i))
-               for i in [0, 127, 128, 255, 4095, *rng.integers(p.Nq, size=35)]]
-    ref_o, ref_lse = attention_rows(q, k, v, p.scale, True, samples)
-    bound, _ = attention_rows(q, k, np.abs(v), p.scale, True, samples)
-    got_o = np.stack([o[b, h, i] for b, h, i in samples])
-    got_l = np.array([lse[b, h, i] for b, h, i in samples])
-    _check(got_o, got_l, ref_o, ref_lse, bound, "fp8 headline (sampled)")
+    g = p.Hq // p.Hkv
+    for b in range(p.B):
+        for h in range(p.Hq):
+            kq, kk = (b, h), (b, h // g)
+            qs, ks, vs = q[kq[0]:kq[0] + 1, kq[1]:kq[1] + 1], k[kk[0]:kk[0] + 1, kk[1]:kk[1] + 1], \
+                v[kk[0]:kk[0] + 1, kk[1]:kk[1] + 1]
+            ref_o, ref_lse = attention_fwd(qs, ks, vs, p.scale, True)
+            bound, _ = attention_fwd(qs, ks, np.abs(vs), p.scale, True)
+            _check(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], ref_o, ref_lse, bound,
+                   "fp8 headline b=%d h=%d" % (b, h))

@@ -130,3 +130,38 @@ def test_rotation_lowers_the_error_with_outlier_channels(fa, dev):
         rms[rotate] = math.sqrt(float(np.mean(err ** 2)))
     assert rms[True] < 0.6 * rms[False], rms
     assert rms[True] < 6e-3, rms
+
+
+def test_non_finite_inputs_follow_the_documented_rule(fa, dev):
+    """fa.h states what a NaN or an infinity does to the codes (unrotated):
+    a NaN is left out of its slice's maximum and gets a NaN code; an infinity
+    makes the slice's descale +inf, its own code NaN and every other code of
+    the slice a zero.  Slices without a non-finite element match the oracle."""
+    B, H, N, d = 1, 3, 128, 128
+    bits = normal_bf16(stream_key(411, 1), (B, H, N, d))
+    nan_at, inf_at = (0, 0, 5, 17), (0, 1, 70, 3)
+    bits[nan_at] = 0x7FC0   # bf16 quiet NaN
+    bits[inf_at] = 0xFF80   # bf16 -inf
+    x8, desc = fa.fp8_quantize(_to_dev(bits, dev), None)
+    torch.cuda.synchronize(dev)
+    got8, got_d = x8.cpu().numpy(), desc.cpu().numpy()
+    is_nan_code = lambda c: (c & 0x7F) == 0x7F
+    # Slice 0: the NaN element's code is NaN; the rest are the codes of the
+    # same slice with that element set to 0 (it is left out of the maximum).
+    assert is_nan_code(got8[nan_at])
+    clean = bits.copy()
+    clean[nan_at] = 0
+    clean[inf_at] = 0       # slice 1 is checked against the rule below, not the oracle
+    ref8, ref_d = fp8_quantize(bf16_bits_to_f32(clean), None)
+    mask = np.ones(got8[0, 0].shape, dtype=bool)
+    mask[nan_at[2:]] = False
+    assert np.array_equal(got8[0, 0][mask], ref8[0, 0][mask])
+    assert got_d[0, 0] == ref_d[0, 0]
+    # Slice 1: descale +inf, the infinity's code NaN, every other code a zero.
+    assert np.isposinf(got_d[0, 1])
+    assert is_nan_code(got8[inf_at])
+    rest = np.ones(got8[0, 1].shape, dtype=bool)
+    rest[inf_at[2:]] = False
+    assert np.all((got8[0, 1][rest] & 0x7F) == 0)
+    # Slice 2 is untouched by the others.
+    assert np.array_equal(got8[0, 2], ref8[0, 2]) and got_d[0, 2] == ref_d[0, 2]
