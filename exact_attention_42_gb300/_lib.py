@@ -47,6 +47,8 @@ def lib() -> ctypes.CDLL:
             L.fa_fwd_threads.restype = ci
             L.fa_debug_fault_injection.argtypes = [ci, ctypes.c_double]
             L.fa_debug_fault_injection.restype = ci
+            L.fa_debug_fwd_pair.argtypes = [ci]
+            L.fa_debug_fwd_pair.restype = ci
             L.fa_debug_soft_exp.argtypes = [ci]
             L.fa_debug_soft_exp.restype = ci
             L.fa_debug_exp2_soft.argtypes = [vp, vp, ci, vp]
@@ -126,6 +128,13 @@ def fa_debug_soft_exp(on: int) -> None:
     st = lib().fa_debug_soft_exp(int(on))
     if st != 0:
         raise FaError(st, "fa_debug_soft_exp")
+
+
+def fa_debug_fwd_pair(on: int) -> None:
+    """Test hook: 1 selects the CTA-pair forward kernel for bf16, d = 128 (see fa.h)."""
+    st = lib().fa_debug_fwd_pair(int(on))
+    if st != 0:
+        raise FaError(st, "fa_debug_fwd_pair")
 
 
 def fa_debug_exp2_soft(x_ptr: int, y_ptr: int, n: int, stream: int = 0) -> None:

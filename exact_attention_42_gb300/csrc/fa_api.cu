@@ -25,6 +25,7 @@ struct DeviceInfo {
 static std::atomic<int> g_fault_mode{0};
 static std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
 static std::atomic<int> g_soft_exp{0};
+static std::atomic<int> g_fwd_pair{0};
 
 static DeviceInfo g_dev[kMaxDevicesDecode];
 static std::mutex g_dev_mutex;
@@ -52,6 +53,7 @@ static fa_status launch_env(LaunchEnv* env) {
   env->wait_limit_ns = g_wait_limit_ns.load();
   env->fault_mode = g_fault_mode.load();
   env->soft_exp = g_soft_exp.load();
+  env->fwd_pair = g_fwd_pair.load();
   return FA_OK;
 }
 
@@ -220,6 +222,12 @@ fa_status fa_debug_fault_injection(int mode, double wait_limit_seconds) {
 fa_status fa_debug_soft_exp(int on) {
   if (on != 0 && on != 1) return FA_ERR_VALUE;
   fa::g_soft_exp.store(on);
+  return FA_OK;
+}
+
+fa_status fa_debug_fwd_pair(int on) {
+  if (on != 0 && on != 1) return FA_ERR_VALUE;
+  fa::g_fwd_pair.store(on);
   return FA_OK;
 }
 

@@ -54,7 +54,6 @@ namespace fa {
 constexpr int BLOCK_M = 128;      // query rows per tile (= TMEM lanes)
 constexpr int BLOCK_N = 128;      // keys per K/V tile
 constexpr int NQT = 2;            // query tiles per CTA
-constexpr int UNIT_ROWS = BLOCK_M * NQT;
 constexpr int NUM_THREADS = 384;  // three warpgroups
 constexpr int WARP_PRODUCER = 8;
 constexpr int WARP_MMA = 9;  // issues the products of both query tiles (warp 10 is idle)
@@ -120,23 +119,34 @@ constexpr int SOFT_EXP_PERIOD = 2;
 __device__ int g_fa_status;
 
 // FP8 selects the 8-bit path: e4m3 Q, K and V^T, products of kind f8f6f4.
-template <int D, bool FP8 = false>
+// PAIR selects the CTA-pair path: two CTAs of a cluster share each product
+// (tcgen05 cta_group::2, M = 256), each holding its own 128 query rows of a
+// 256-row product tile and half of every K tile (64 keys) and V tile (64 head
+// dims), so that a K/V tile is read from L2 once per pair and one instruction
+// covers both SMs.
+template <int D, bool FP8 = false, bool PAIR = false>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(!FP8 || D == 128, "the 8-bit path is built for d = 128");
+  static_assert(!PAIR || (D == 128 && !FP8), "the CTA-pair path is built for bf16, d = 128");
   static constexpr int ELEM = FP8 ? 1 : 2;             // bytes per element
   static constexpr int TILE_BYTES = BLOCK_M * D * ELEM;  // one 128 x D tile
   static constexpr int CHUNKS = D * ELEM / 128;        // 128-byte swizzle column blocks
   static constexpr int CHUNK_COLS = 128 / ELEM;        // elements per column block
   static constexpr int CHUNK_BYTES = BLOCK_M * 128;    // 16 KB
-  static constexpr int NS = (TILE_BYTES == 32768) ? 5 : 8;  // K/V ring slots
+  static constexpr int SLOT_BYTES = PAIR ? TILE_BYTES / 2 : TILE_BYTES;  // a pair's CTA holds half a tile
+  static constexpr int NS = PAIR ? 10 : ((TILE_BYTES == 32768) ? 5 : 8);  // K/V ring slots
   static constexpr int QK_KSTEPS = D * ELEM / 32;      // 32 bytes of K per product
   static constexpr int PV_KSTEPS = BLOCK_N * ELEM / 32;
   static constexpr int SMEM_Q = NQT * TILE_BYTES;
-  static constexpr int SMEM_RING = NS * TILE_BYTES;
+  static constexpr int SMEM_RING = NS * SLOT_BYTES;
+  static constexpr int CTAS = PAIR ? 2 : 1;            // CTAs sharing one product tile
+  static constexpr int TILE_ROWS = CTAS * BLOCK_M;     // query rows of one product tile
+  static constexpr int UNIT_ROWS = NQT * TILE_ROWS;    // query rows of one work unit
   // barriers: full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], drain
   static constexpr int NUM_BARS = 2 * NS + (4 + P_PARTS) * NQT + 1;
   static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + NUM_BARS * 8 + 16;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
 struct Params {
@@ -167,10 +177,10 @@ struct Unit {
 
 __device__ __forceinline__ int clampi(int x, int lo, int hi) { return x < lo ? lo : (x > hi ? hi : x); }
 
-// Unit u -> (sequence, head, query block).  Dense units are ordered
-// longest-first under a causal mask: the last query blocks of every head come
-// first, so the persistent CTAs start on the heaviest work.
-__device__ __forceinline__ bool decode_unit(const Params& p, int u, Unit& w) {
+// Unit u -> (sequence, head, query block of unit_rows rows).  Dense units are
+// ordered longest-first under a causal mask: the last query blocks of every
+// head come first, so the persistent CTAs start on the heaviest work.
+__device__ __forceinline__ bool decode_unit(const Params& p, int u, Unit& w, int unit_rows) {
   if (p.cu_seqlens == nullptr) {
     const int bh_count = p.B * p.Hq;
     const int qb = p.nqb - 1 - u / bh_count;
@@ -178,7 +188,7 @@ __device__ __forceinline__ bool decode_unit(const Params& p, int u, Unit& w) {
     const int b = bh / p.Hq, h = bh % p.Hq;
     w.Lq = p.Nq;
     w.Lk = p.Nk;
-    w.row0 = qb * UNIT_ROWS;
+    w.row0 = qb * unit_rows;
     w.q_y = 0;
     w.k_y = 0;
     w.q_z = bh;
@@ -195,11 +205,11 @@ __device__ __forceinline__ bool decode_unit(const Params& p, int u, Unit& w) {
   for (int s = 0; s < p.B; ++s) {
     const int next = clampi(__ldg(p.cu_seqlens + s + 1), prev, T);
     const int L = next - prev;
-    const int nb = (L + UNIT_ROWS - 1) / UNIT_ROWS;
+    const int nb = (L + unit_rows - 1) / unit_rows;
     if (blk < nb) {
       w.Lq = L;
       w.Lk = L;
-      w.row0 = (nb - 1 - blk) * UNIT_ROWS;
+      w.row0 = (nb - 1 - blk) * unit_rows;
       w.q_y = prev;
       w.k_y = prev;
       w.q_z = h;
@@ -213,25 +223,26 @@ __device__ __forceinline__ bool decode_unit(const Params& p, int u, Unit& w) {
   return false;
 }
 
-__device__ __forceinline__ int packed_num_units(const Params& p) {
+__device__ __forceinline__ int packed_num_units(const Params& p, int unit_rows) {
   const int T = p.Nq;
   int prev = clampi(__ldg(p.cu_seqlens), 0, T);
   int total = 0;
   for (int s = 0; s < p.B; ++s) {
     const int next = clampi(__ldg(p.cu_seqlens + s + 1), prev, T);
-    total += (next - prev + UNIT_ROWS - 1) / UNIT_ROWS;
+    total += (next - prev + unit_rows - 1) / unit_rows;
     prev = next;
   }
   return total * p.Hq;
 }
 
-// Number of K/V tiles query tile t of unit w must visit (0: no key visible).
-__device__ __forceinline__ int kv_tiles(const Params& p, const Unit& w, int t) {
-  const int q0 = w.row0 + t * BLOCK_M;
+// Number of K/V tiles product tile t (tile_rows query rows) of unit w must
+// visit (0: no key visible to any of its rows).
+__device__ __forceinline__ int kv_tiles(const Params& p, const Unit& w, int t, int tile_rows) {
+  const int q0 = w.row0 + t * tile_rows;
   if (q0 >= w.Lq || w.Lk <= 0) return 0;
   int last_key = w.Lk - 1;
   if (p.causal) {
-    const int last_row = min(q0 + BLOCK_M - 1, w.Lq - 1);
+    const int last_row = min(q0 + tile_rows - 1, w.Lq - 1);
     last_key = min(last_key, last_row + (w.Lk - w.Lq));
     if (last_key < 0) return 0;
   }
@@ -283,32 +294,43 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
                : "memory");
 }
 
-__device__ __forceinline__ void raise_abort(volatile int* abort_flag, int role) {
-  *abort_flag = 1;
-  atomicOr(&g_fa_status, 1 << role);
-}
+// The CTA's abort flag and, on the CTA-pair path, the other CTA's flag: a role
+// that gives up stops both CTAs of the pair, since each waits on the other.
+struct Abort {
+  volatile int* flag;
+  uint32_t partner;  // cluster address of the other CTA's flag (pair path only)
+  bool pair;
+  __device__ __forceinline__ void raise(int role) const {
+    *flag = 1;
+    if (pair) st_cluster_u32(partner, 1u);
+    atomicOr(&g_fa_status, 1 << role);
+  }
+};
 
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                              int role, uint64_t limit_ns) {
-  if (mbar_wait(bar, parity, abort_flag, limit_ns)) return true;
-  if (!*abort_flag) raise_abort(abort_flag, role);
+// Bounded wait; `cluster` selects acquire semantics at cluster scope (for
+// barriers that the other CTA of a pair also signals).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const Abort& ab, int role,
+                                              uint64_t limit_ns, bool cluster = false) {
+  if (cluster ? mbar_wait_cluster(bar, parity, ab.flag, limit_ns) : mbar_wait(bar, parity, ab.flag, limit_ns))
+    return true;
+  if (!*ab.flag) ab.raise(role);
   return false;
 }
 
 // Teardown waits ignore the abort flag: they only wait for copies and MMAs
 // that were already issued, which complete on their own.
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, volatile int* abort_flag, int role,
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, const Abort& ab, int role,
                                            uint64_t limit_ns) {
   __shared__ int never;
   never = 0;
-  if (!mbar_wait(bar, parity, &never, limit_ns)) raise_abort(abort_flag, role);
+  if (!mbar_wait_cluster(bar, parity, &never, limit_ns)) ab.raise(role);
 }
 
-template <int D, bool FP8, int SOFT>
+template <int D, bool FP8, int SOFT, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  using C = Cfg<D, FP8>;
+  using C = Cfg<D, FP8, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -332,6 +354,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
+  // Pair path: CTA rank 0 of the cluster issues the products of both CTAs;
+  // the full, q_full and P barriers that the issuer waits on live in its
+  // shared memory and count the other CTA's copies and arrivals too.
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  auto leader_bar = [&](uint32_t bar) { return PAIR ? cluster_addr(bar, 0) : bar; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::NS; ++s) {
@@ -342,8 +369,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(qfull_bar(t), 1);
       mbar_init(qempty_bar(t), 1);
       mbar_init(sfull_bar(t), 1);
-      mbar_init(pfull_bar(t), BLOCK_M / 32);  // one arrival per softmax warp
-      for (int i = 0; i + 1 < P_PARTS; ++i) mbar_init(ppart_bar(t, i), BLOCK_M / 32);
+      mbar_init(pfull_bar(t), C::CTAS * BLOCK_M / 32);  // one arrival per softmax warp of the pair
+      for (int i = 0; i + 1 < P_PARTS; ++i) mbar_init(ppart_bar(t, i), C::CTAS * BLOCK_M / 32);
       mbar_init(odone_bar(t), 1);
     }
     mbar_init(drain_bar, 1);
@@ -351,23 +378,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     fence_mbar_init();
   }
   if (warp == WARP_MMA) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), 512);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), 512);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync_all();  // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, PAIR ? cluster_addr(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u) : 0u, PAIR};
 
-  const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_num_units(p);
-  // Static "snake" schedule: in round k the CTAs take units [k*G, (k+1)*G) in
-  // alternating directions, so the longest-first unit list is spread evenly
-  // (with the 1:16 cost range of a causal head the busiest CTA stays within a
-  // few percent of the mean, against 13% for plain round-robin).
-  auto snake_unit = [&](int k) {
-    const int g = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-    return k * g + ((k & 1) ? (g - 1 - c) : c);
-  };
+  const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_num_units(p, C::UNIT_ROWS);
+  // Static "snake" schedule over the grid's G persistent workers (CTAs, or
+  // CTA pairs on the pair path): in round k the workers take units
+  // [k*G, (k+1)*G) in alternating directions, so the longest-first unit list
+  // is spread evenly (with the 1:16 cost range of a causal head the busiest
+  // worker stays within a few percent of the mean, against 13% for plain
+  // round-robin).
+  const int G = static_cast<int>(gridDim.x) / C::CTAS;
+  const int worker = static_cast<int>(blockIdx.x) / C::CTAS;
+  auto snake_unit = [&](int k) { return k * G + ((k & 1) ? (G - 1 - worker) : worker); };
+  auto tiles_of = [&](const Unit& w, int t) { return kv_tiles(p, w, t, C::TILE_ROWS); };
 
   if (warp >= 8) {
   setmaxnreg_dec<REG_OTHER>();
@@ -386,59 +422,83 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // current unit ends hides most of that latency at the unit boundary.
       auto prefetch_next_unit = [&](int k_next) {
         const int un = snake_unit(k_next);
-        if (k_next * static_cast<int>(gridDim.x) >= num_units || un >= num_units) return;
+        if (k_next * G >= num_units || un >= num_units) return;
         Unit wn;
-        if (!decode_unit(p, un, wn)) return;
-        const int nk0 = kv_tiles(p, wn, 0), nk1 = kv_tiles(p, wn, 1);
+        if (!decode_unit(p, un, wn, C::UNIT_ROWS)) return;
+        const int nk0 = tiles_of(wn, 0), nk1 = tiles_of(wn, 1);
         for (int t = 0; t < NQT; ++t) {
           if ((t == 0 ? nk0 : nk1) == 0) continue;
           for (int c = 0; c < C::CHUNKS; ++c)
-            tma_prefetch_l2_3d(&tm_q, c * C::CHUNK_COLS, wn.q_y + wn.row0 + t * BLOCK_M, wn.q_z);
+            tma_prefetch_l2_3d(&tm_q, c * C::CHUNK_COLS, wn.q_y + wn.row0 + t * C::TILE_ROWS + rank * BLOCK_M,
+                               wn.q_z);
         }
         const int nn = min(max(nk0, nk1), PREFETCH_KV_TILES);
         for (int j = 0; j < nn; ++j)
           for (int c = 0; c < C::CHUNKS; ++c) {
-            tma_prefetch_l2_3d(&tm_k, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
-            if constexpr (FP8)  // V^T: keys along x, head dims along y
-              tma_prefetch_l2_3d(&tm_v, wn.k_y + j * BLOCK_N, 0, wn.k_z);
-            else
-              tma_prefetch_l2_3d(&tm_v, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
+            if constexpr (PAIR) {  // this CTA's halves: keys [64 rank, +64) of K, columns [64 rank, +64) of V
+              tma_prefetch_l2_3d(&tm_k, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N + rank * (BLOCK_N / 2), wn.k_z);
+              if (c == 0) tma_prefetch_l2_3d(&tm_v, rank * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
+            } else {
+              tma_prefetch_l2_3d(&tm_k, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
+              if constexpr (FP8)  // V^T: keys along x, head dims along y
+                tma_prefetch_l2_3d(&tm_v, wn.k_y + j * BLOCK_N, 0, wn.k_z);
+              else
+                tma_prefetch_l2_3d(&tm_v, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
+            }
           }
       };
-      for (int k = 0; k * static_cast<int>(gridDim.x) < num_units && ok; ++k) {
+      for (int k = 0; k * G < num_units && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= num_units) continue;
         Unit w;
-        if (!decode_unit(p, u, w)) continue;
-        const int nmax = max(kv_tiles(p, w, 0), kv_tiles(p, w, 1));
+        if (!decode_unit(p, u, w, C::UNIT_ROWS)) continue;
+        const int nmax = max(tiles_of(w, 0), tiles_of(w, 1));
         if (nmax <= PREFETCH_LEAD) prefetch_next_unit(k + 1);
         for (int j = 0; j < nmax && ok; ++j) {
           if (j == nmax - PREFETCH_LEAD) prefetch_next_unit(k + 1);
           for (int kv = 0; kv < 2; ++kv) {
             const int s = it % C::NS;
-            if (!(ok = wait_or_abort(empty_bar(s), ((it / C::NS) & 1u) ^ 1u, abort_flag, 0, p.wait_limit_ns))) break;
+            if (!(ok = wait_or_abort(empty_bar(s), ((it / C::NS) & 1u) ^ 1u, ab, 0, p.wait_limit_ns, PAIR))) break;
             if (p.fault_inject == 1 && it == 0) {  // test hook: this fill never arrives
               ++it;
               continue;
             }
-            mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
-            const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
-            if (FP8 && kv) {  // V^T tile: 128 head dims (rows) x 128 keys (bytes)
-              tma_load_3d(dst, &tm_v, full_bar(s), w.k_y + j * BLOCK_N, 0, w.k_z);
+            const uint32_t dst = smem_u32(sRing + s * C::SLOT_BYTES);
+            if constexpr (PAIR) {
+              // Both CTAs' halves are counted on the even CTA's full barrier,
+              // which that CTA arms for the whole tile.
+              const uint32_t fb = leader_bar(full_bar(s));
+              if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * C::SLOT_BYTES);
+              if (kv == 0) {  // K: keys [64 rank, +64) of the tile, every head dim
+                for (int c = 0; c < C::CHUNKS; ++c)
+                  tma_load_3d_pair(dst + c * (C::SLOT_BYTES / C::CHUNKS), &tm_k, fb, c * C::CHUNK_COLS,
+                                   w.k_y + j * BLOCK_N + rank * (BLOCK_N / 2), w.k_z);
+              } else {        // V: head dims [64 rank, +64) of every key of the tile
+                tma_load_3d_pair(dst, &tm_v, fb, rank * C::CHUNK_COLS, w.k_y + j * BLOCK_N, w.k_z);
+              }
             } else {
-              for (int c = 0; c < C::CHUNKS; ++c)
-                tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, full_bar(s), c * C::CHUNK_COLS,
-                            w.k_y + j * BLOCK_N, w.k_z);
+              mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
+              if (FP8 && kv) {  // V^T tile: 128 head dims (rows) x 128 keys (bytes)
+                tma_load_3d(dst, &tm_v, full_bar(s), w.k_y + j * BLOCK_N, 0, w.k_z);
+              } else {
+                for (int c = 0; c < C::CHUNKS; ++c)
+                  tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, full_bar(s), c * C::CHUNK_COLS,
+                              w.k_y + j * BLOCK_N, w.k_z);
+              }
             }
             ++it;
           }
         }
       }
-      // Wait until every issued copy has landed before the CTA may exit.
-      for (int s = 0; s < C::NS; ++s) {
-        if (it > static_cast<uint32_t>(s)) {
-          const uint32_t f = s + C::NS * ((it - 1 - s) / C::NS);
-          wait_drain(full_bar(s), (f / C::NS) & 1u, abort_flag, 0, p.wait_limit_ns);
+      // Wait until every issued copy has landed before the CTA may exit.  On
+      // the pair path the even CTA's full barriers count both CTAs' copies;
+      // the odd CTA cannot observe them and relies on the teardown below.
+      if (!PAIR || rank == 0) {
+        for (int s = 0; s < C::NS; ++s) {
+          if (it > static_cast<uint32_t>(s)) {
+            const uint32_t f = s + C::NS * ((it - 1 - s) / C::NS);
+            wait_drain(full_bar(s), (f / C::NS) & 1u, ab, 0, p.wait_limit_ns);
+          }
         }
       }
     }
@@ -447,28 +507,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t qfills[NQT] = {0, 0};
       bool ok = true;
-      for (int k = 0; k * static_cast<int>(gridDim.x) < num_units && ok; ++k) {
+      for (int k = 0; k * G < num_units && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= num_units) continue;
         Unit w;
-        if (!decode_unit(p, u, w)) continue;
+        if (!decode_unit(p, u, w, C::UNIT_ROWS)) continue;
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
-          if (!ok || kv_tiles(p, w, t) == 0) continue;
-          if (!(ok = wait_or_abort(qempty_bar(t), (qfills[t] & 1u) ^ 1u, abort_flag, 4, p.wait_limit_ns))) continue;
-          mbar_arrive_expect_tx(qfull_bar(t), C::TILE_BYTES);
+          if (!ok || tiles_of(w, t) == 0) continue;
+          if (!(ok = wait_or_abort(qempty_bar(t), (qfills[t] & 1u) ^ 1u, ab, 4, p.wait_limit_ns, PAIR))) continue;
           const uint32_t dst = smem_u32(sQ + t * C::TILE_BYTES);
-          for (int c = 0; c < C::CHUNKS; ++c)
-            tma_load_3d(dst + c * C::CHUNK_BYTES, &tm_q, qfull_bar(t), c * C::CHUNK_COLS,
-                        w.q_y + w.row0 + t * BLOCK_M, w.q_z);
+          const int row = w.q_y + w.row0 + t * C::TILE_ROWS + static_cast<int>(rank) * BLOCK_M;
+          if constexpr (PAIR) {
+            if (rank == 0) mbar_arrive_expect_tx(qfull_bar(t), 2 * C::TILE_BYTES);
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_3d_pair(dst + c * C::CHUNK_BYTES, &tm_q, leader_bar(qfull_bar(t)), c * C::CHUNK_COLS, row,
+                               w.q_z);
+          } else {
+            mbar_arrive_expect_tx(qfull_bar(t), C::TILE_BYTES);
+            for (int c = 0; c < C::CHUNKS; ++c)
+              tma_load_3d(dst + c * C::CHUNK_BYTES, &tm_q, qfull_bar(t), c * C::CHUNK_COLS, row, w.q_z);
+          }
           ++qfills[t];
         }
       }
+      if (!PAIR || rank == 0) {
 #pragma unroll
-      for (int t = 0; t < NQT; ++t)
-        if (qfills[t] > 0) wait_drain(qfull_bar(t), (qfills[t] - 1) & 1u, abort_flag, 4, p.wait_limit_ns);
+        for (int t = 0; t < NQT; ++t)
+          if (qfills[t] > 0) wait_drain(qfull_bar(t), (qfills[t] - 1) & 1u, ab, 4, p.wait_limit_ns);
+      }
     }
-  } else if (warp == WARP_MMA) {
+  } else if (warp == WARP_MMA && (!PAIR || rank == 0)) {
     // ------------------------------------------------------------------ MMA
     // Per tile the order is QK(0), then for each j: PV(j), QK(j+1); S_t is
     // therefore overwritten by QK(j+1) only after PV(j) has read the P that
@@ -477,22 +546,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}" : "=r"(elected));
     const bool leader = elected != 0;
     // 8-bit path: both products K-major (V arrives transposed), 32 bytes of K each.
-    constexpr uint32_t IDESC_QK = FP8 ? idesc_e4m3_f32(BLOCK_M, BLOCK_N) : idesc_bf16_f32(BLOCK_M, BLOCK_N, 0, 0);
-    constexpr uint32_t IDESC_PV = FP8 ? idesc_e4m3_f32(BLOCK_M, D) : idesc_bf16_f32(BLOCK_M, D, 0, 1);
+    constexpr uint32_t IDESC_QK =
+        FP8 ? idesc_e4m3_f32(BLOCK_M, BLOCK_N) : idesc_bf16_f32(C::TILE_ROWS, BLOCK_N, 0, 0);
+    constexpr uint32_t IDESC_PV = FP8 ? idesc_e4m3_f32(BLOCK_M, D) : idesc_bf16_f32(C::TILE_ROWS, D, 0, 1);
     const uint32_t q_addr = smem_u32(sQ);
     const uint32_t ring_addr = smem_u32(sRing);
+    // Byte stride between the 128-byte-wide column blocks of a K slot: a full
+    // 128-row tile, or the 64-key half a CTA of a pair holds.
+    constexpr int K_CHUNK_BYTES = C::SLOT_BYTES / C::CHUNKS;
     // S_t = Q_t K^T: both operands K-major (head dim contiguous), 16 columns per MMA.
     auto issue_qk = [&](int t, int slot) {
       const uint64_t q_desc = smem_desc_sw128(q_addr + t * C::TILE_BYTES, 16, 1024);
-      const uint64_t k_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, 16, 1024);
+      const uint64_t k_desc = smem_desc_sw128(ring_addr + slot * C::SLOT_BYTES, 16, 1024);
 #pragma unroll
       for (int kk = 0; kk < C::QK_KSTEPS; ++kk) {
-        const uint64_t off = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
+        const uint64_t qoff = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
+        const uint64_t koff = static_cast<uint64_t>((kk / 4) * K_CHUNK_BYTES + (kk % 4) * 32) >> 4;
         if (leader) {
           if constexpr (FP8)
-            umma_ss_f8(tmem + t * 128, q_desc + off, k_desc + off, IDESC_QK, kk > 0 ? 1u : 0u);
+            umma_ss_f8(tmem + t * 128, q_desc + qoff, k_desc + koff, IDESC_QK, kk > 0 ? 1u : 0u);
+          else if constexpr (PAIR)
+            umma_ss_pair(tmem + t * 128, q_desc + qoff, k_desc + koff, IDESC_QK, kk > 0 ? 1u : 0u);
           else
-            umma_ss(tmem + t * 128, q_desc + off, k_desc + off, IDESC_QK, kk > 0 ? 1u : 0u);
+            umma_ss(tmem + t * 128, q_desc + qoff, k_desc + koff, IDESC_QK, kk > 0 ? 1u : 0u);
         }
       }
     };
@@ -500,7 +576,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto issue_pv = [&](int t, int slot, bool accumulate, int part) {
       if constexpr (FP8) {
         // V^T K-major (keys contiguous); P as packed e4m3 in TMEM, 8 columns per 32 keys.
-        const uint64_t vt_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, 16, 1024);
+        const uint64_t vt_desc = smem_desc_sw128(ring_addr + slot * C::SLOT_BYTES, 16, 1024);
 #pragma unroll
         for (int kk = part * C::PV_KSTEPS / P_PARTS; kk < (part + 1) * C::PV_KSTEPS / P_PARTS; ++kk) {
           if (leader)
@@ -508,46 +584,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                        IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
         }
       } else {
-        const uint64_t v_desc = smem_desc_sw128(ring_addr + slot * C::TILE_BYTES, C::CHUNK_BYTES, 1024);
+        // On the pair path each CTA's slot holds one 128-byte column block
+        // (64 head dims) of V; the stride between blocks is then unused.
+        const uint64_t v_desc = smem_desc_sw128(ring_addr + slot * C::SLOT_BYTES, C::CHUNK_BYTES, 1024);
 #pragma unroll
         for (int kk = part * BLOCK_N / (16 * P_PARTS); kk < (part + 1) * BLOCK_N / (16 * P_PARTS); ++kk) {
-          if (leader)
-            umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                    v_desc + static_cast<uint64_t>(kk * 16 * 128 >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+          if (leader) {
+            if constexpr (PAIR)
+              umma_ts_pair(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                           v_desc + static_cast<uint64_t>(kk * 16 * 128 >> 4), IDESC_PV,
+                           (accumulate || kk > 0) ? 1u : 0u);
+            else
+              umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                      v_desc + static_cast<uint64_t>(kk * 16 * 128 >> 4), IDESC_PV, (accumulate || kk > 0) ? 1u : 0u);
+          }
         }
       }
     };
+    // Signals a barrier that both CTAs of a pair wait on (the same barrier in
+    // each CTA), or the CTA's own barrier.
     auto commit = [&](uint32_t bar) {
-      if (leader) umma_commit(bar);
+      if (leader) {
+        if constexpr (PAIR) {
+          umma_commit_pair(bar);
+          umma_commit_pair(cluster_addr(bar, 1));
+        } else {
+          umma_commit(bar);
+        }
+      }
       __syncwarp();
     };
     uint32_t it = 0;
     uint32_t qcnt[NQT] = {0, 0}, pcnt[NQT] = {0, 0};
     bool ok = true;
-    for (int k = 0; k * static_cast<int>(gridDim.x) < num_units && ok; ++k) {
+    for (int k = 0; k * G < num_units && ok; ++k) {
       const int u = snake_unit(k);
       if (u >= num_units) continue;
       Unit w;
-      if (!decode_unit(p, u, w)) continue;
+      if (!decode_unit(p, u, w, C::UNIT_ROWS)) continue;
       int nkv[NQT];
       int nmax = 0;
 #pragma unroll
       for (int t = 0; t < NQT; ++t) {
-        nkv[t] = kv_tiles(p, w, t);
+        nkv[t] = tiles_of(w, t);
         nmax = max(nmax, nkv[t]);
       }
       if (nmax == 0) continue;
 #pragma unroll
       for (int t = 0; t < NQT; ++t) {
         if (!ok || nkv[t] == 0) continue;
-        ok = wait_or_abort(qfull_bar(t), qcnt[t] & 1u, abort_flag, 1, p.wait_limit_ns);
+        ok = wait_or_abort(qfull_bar(t), qcnt[t] & 1u, ab, 1, p.wait_limit_ns, PAIR);
         ++qcnt[t];
       }
       if (!ok) break;
       // K_0 for every active tile.
       {
         const int s = it % C::NS;
-        if (!(ok = wait_or_abort(full_bar(s), (it / C::NS) & 1u, abort_flag, 1, p.wait_limit_ns))) break;
+        if (!(ok = wait_or_abort(full_bar(s), (it / C::NS) & 1u, ab, 1, p.wait_limit_ns, PAIR))) break;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < NQT; ++t) {
@@ -561,7 +654,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       for (int j = 0; j < nmax && ok; ++j) {
         const int sv = it % C::NS;
-        if (!(ok = wait_or_abort(full_bar(sv), (it / C::NS) & 1u, abort_flag, 1, p.wait_limit_ns))) break;
+        if (!(ok = wait_or_abort(full_bar(sv), (it / C::NS) & 1u, ab, 1, p.wait_limit_ns, PAIR))) break;
         tc_fence_after();
         ++it;
         const bool has_next = j + 1 < nmax;
@@ -575,7 +668,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < P_PARTS && ok; ++i) {
             const uint32_t bar = (i + 1 < P_PARTS) ? ppart_bar(t, i) : pfull_bar(t);
-            if (!(ok = wait_or_abort(bar, pcnt[t] & 1u, abort_flag, 1, p.wait_limit_ns))) break;
+            if (!(ok = wait_or_abort(bar, pcnt[t] & 1u, ab, 1, p.wait_limit_ns, PAIR))) break;
             tc_fence_after();
             issue_pv(t, sv, j > 0 || i > 0, i);
           }
@@ -584,7 +677,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (j + 1 == nkv[t]) commit(odone_bar(t));  // last PV of this tile in the unit
           if (j + 1 < nkv[t]) {
             if (!k_ready) {
-              if (!(ok = wait_or_abort(full_bar(sk), (it / C::NS) & 1u, abort_flag, 1, p.wait_limit_ns))) continue;
+              if (!(ok = wait_or_abort(full_bar(sk), (it / C::NS) & 1u, ab, 1, p.wait_limit_ns, PAIR))) continue;
               tc_fence_after();
               k_ready = true;
             }
@@ -602,8 +695,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
     // Every MMA issued so far completes before the CTA may release TMEM.
-    commit(drain_bar);
-    wait_drain(drain_bar, 0, abort_flag, 1, p.wait_limit_ns);
+    if (leader) {
+      if constexpr (PAIR)
+        umma_commit_pair(drain_bar);
+      else
+        umma_commit(drain_bar);
+    }
+    __syncwarp();
+    wait_drain(drain_bar, 0, ab, 1, p.wait_limit_ns);
   }
   } else {
     setmaxnreg_inc<REG_SOFTMAX>();
@@ -617,16 +716,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float NEG_INF = -INFINITY;
     constexpr float tau = FP8 ? TAU_FP8 : TAU;
     constexpr float p_shift = FP8 ? P_SHIFT_FP8 : 0.f;
+    // One arrival per warp on a P barrier of the issuing CTA.  On the pair
+    // path the arrival is relaxed: the data it announces is in TMEM, complete
+    // once tcgen05.wait::st returns and ordered by tcgen05.fence::before_thread_sync,
+    // and no shared- or global-memory write has to be released with it.  A
+    // release at cluster scope measured about 900 cycles per arrival on GB300
+    // (against about 50), which doubled the softmax's time per K/V tile.
+    auto arrive_p = [&](uint32_t bar) {
+      if constexpr (PAIR)
+        mbar_arrive_remote_relaxed(leader_bar(bar));
+      else
+        mbar_arrive(bar);
+    };
     uint32_t scnt = 0, ocnt = 0;
     bool ok = true;
-    for (int k = 0; k * static_cast<int>(gridDim.x) < num_units && ok; ++k) {
-        const int u = snake_unit(k);
-        if (u >= num_units) continue;
+    for (int k = 0; k * G < num_units && ok; ++k) {
+      const int u = snake_unit(k);
+      if (u >= num_units) continue;
       Unit w;
-      if (!decode_unit(p, u, w)) continue;
-      const int q0 = w.row0 + t * BLOCK_M;
-      if (q0 >= w.Lq) continue;
-      const int nkv = kv_tiles(p, w, t);
+      if (!decode_unit(p, u, w, C::UNIT_ROWS)) continue;
+      // This CTA's 128 rows of product tile t.
+      const int q0 = w.row0 + t * C::TILE_ROWS + static_cast<int>(rank) * BLOCK_M;
+      const int nkv = tiles_of(w, t);
+      // On the pair path a CTA whose rows all lie past the sequence end still
+      // takes part in the tile's steps (the products are shared); it stores nothing.
+      if (q0 >= w.Lq && (!PAIR || nkv == 0)) continue;
       const int row = q0 + r;
       const bool row_ok = row < w.Lq;
       const int diag = row + (w.Lk - w.Lq);  // last visible key under the causal mask
@@ -637,7 +751,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float m_used = NEG_INF;
       float l = 0.f;
       for (int j = 0; j < nkv; ++j) {
-        if (!(ok = wait_or_abort(sfull_bar(t), scnt & 1u, abort_flag, 2 + t, p.wait_limit_ns))) break;
+        if (!(ok = wait_or_abort(sfull_bar(t), scnt & 1u, ab, 2 + t, p.wait_limit_ns, PAIR))) break;
         ++scnt;
         tc_fence_after();
         float s[BLOCK_N];
@@ -734,13 +848,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(ppart_bar(t, c0 / 32 / CHUNKS_PER_PART));
+            if (lane == 0) arrive_p(ppart_bar(t, c0 / 32 / CHUNKS_PER_PART));
           }
         }
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(pfull_bar(t));
+        if (lane == 0) arrive_p(pfull_bar(t));
         {
           const float2 a01 = add2(acc[0], acc[1]);
           const float2 a23 = add2(acc[2], acc[3]);
@@ -751,7 +865,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
       if (nkv > 0) {
-        if (!(ok = wait_or_abort(odone_bar(t), ocnt & 1u, abort_flag, 2 + t, p.wait_limit_ns))) break;
+        if (!(ok = wait_or_abort(odone_bar(t), ocnt & 1u, ab, 2 + t, p.wait_limit_ns, PAIR))) break;
         ++ocnt;
         tc_fence_after();
       }
@@ -787,10 +901,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // -------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) {
+    // The products of the even CTA read the odd CTA's shared memory and write
+    // its TMEM, and the odd CTA's copies are counted in the even CTA's
+    // barriers: neither CTA leaves (or frees TMEM) before the other is done.
+    // After a time-out, copies issued by the odd CTA that the even CTA no
+    // longer waits for are given a fixed 0.5 ms to land first.
+    cluster_sync_all();
+    if (*abort_flag && threadIdx.x == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < 500000ull) {
+      }
+    }
+    __syncthreads();
+    cluster_sync_all();
+  }
   if (warp == WARP_MMA) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem, 512);
+    else
+      tmem_dealloc(tmem, 512);
   }
 }
 
@@ -847,19 +979,39 @@ static bool encode_rows_map(CUtensorMap* map, const void* base, int d, long long
 }
 
 // Raises the dynamic shared-memory limit of one kernel instantiation, once
-// per device (the attribute applies to the current device).
-template <int D, bool FP8, int SOFT>
-static bool prepare_kernel(int device) {
+// per device (the attribute applies to the current device).  For the
+// CTA-pair instantiation it also finds how many CTA pairs can be resident at
+// once (*pairs); 0 if none.
+template <int D, bool FP8, int SOFT, bool PAIR>
+static bool prepare_kernel(int device, int* pairs = nullptr) {
   static std::mutex mu;
   static bool attr_set[kMaxDevicesDecode] = {};
+  static int max_pairs[kMaxDevicesDecode] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (device < 0 || device >= kMaxDevicesDecode) return false;
   if (!attr_set[device]) {
-    if (cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, SOFT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<D, FP8>::SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(fa_fwd_kernel<D, FP8, SOFT, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<D, FP8, PAIR>::SMEM_BYTES) != cudaSuccess)
       return false;
+    if (PAIR) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2, 1, 1);
+      cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = Cfg<D, FP8, PAIR>::SMEM_BYTES;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, fa_fwd_kernel<D, FP8, SOFT, PAIR>, &cfg) != cudaSuccess) return false;
+      max_pairs[device] = n;
+    }
     attr_set[device] = true;
   }
+  if (pairs) *pairs = max_pairs[device];
   return true;
 }
 
@@ -871,22 +1023,35 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
     return launch_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, D, scale, causal, stream, env.sms, env.wait_limit_ns,
                          env.fault_mode);
   const bool soft = env.soft_exp != 0;
-  if (!(soft ? prepare_kernel<D, false, SOFT_EXP_PERIOD>(env.device) : prepare_kernel<D, false, 0>(env.device)))
+  // The CTA-pair kernel runs bf16 problems with d = 128 only when the
+  // fa_debug_fwd_pair hook selects it: on GB300 it measured slower than the
+  // single-CTA kernel (the step is set by the MMA issuer and the per-tile
+  // softmax chain, and a pair has one issuer for two SMs).
+  int pairs = 0;
+  bool pair = false;
+  if constexpr (D == 128) {
+    if (env.fwd_pair && !soft) {
+      if (!prepare_kernel<D, false, 0, true>(env.device, &pairs)) return FA_ERR_CUDA;
+      pair = pairs > 0;
+    }
+  }
+  if (!pair && !(soft ? prepare_kernel<D, false, SOFT_EXP_PERIOD, false>(env.device)
+                      : prepare_kernel<D, false, 0, false>(env.device)))
     return FA_ERR_CUDA;
   const bool packed = cu_seqlens != nullptr;
+  const long long q_heads = packed ? Hq : static_cast<long long>(B) * Hq;
+  const long long kv_heads = packed ? Hkv : static_cast<long long>(B) * Hkv;
   alignas(64) CUtensorMap tq, tk, tv;
   std::memset(&tq, 0, sizeof(tq));
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
-  if (packed) {
-    if (!encode_rows_map(&tq, q, D, Nq, Hq)) return FA_ERR_CUDA;
-    if (Nk > 0 && (!encode_rows_map(&tk, k, D, Nk, Hkv) || !encode_rows_map(&tv, v, D, Nk, Hkv))) return FA_ERR_CUDA;
-  } else {
-    if (!encode_rows_map(&tq, q, D, Nq, static_cast<long long>(B) * Hq)) return FA_ERR_CUDA;
-    if (Nk > 0 && (!encode_rows_map(&tk, k, D, Nk, static_cast<long long>(B) * Hkv) ||
-                   !encode_rows_map(&tv, v, D, Nk, static_cast<long long>(B) * Hkv)))
-      return FA_ERR_CUDA;
-  }
+  if (!encode_rows_map(&tq, q, D, Nq, q_heads)) return FA_ERR_CUDA;
+  // A CTA of a pair loads 64-key halves of K tiles.
+  if (Nk > 0 && (!encode_bf16_rows_map(&tk, k, D, Nk, kv_heads, pair ? BLOCK_N / 2 : BLOCK_N) ||
+                 !encode_rows_map(&tv, v, D, Nk, kv_heads)))
+    return FA_ERR_CUDA;
+  const int unit_rows = (pair ? 2 : 1) * NQT * BLOCK_M;  // Cfg<D, false, pair>::UNIT_ROWS
+  const long long workers = pair ? pairs : env.sms;
   Params prm;
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
@@ -902,26 +1067,46 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
   prm.wait_limit_ns = env.wait_limit_ns;
   prm.fault_inject = env.fault_mode == kFaultFwd ? 1 : 0;
   prm.q_descale = prm.k_descale = prm.v_descale = nullptr;
-  long long grid;
+  long long grid;  // persistent workers: CTAs, or CTA pairs
   if (packed) {
     prm.nqb = 0;
     prm.num_units = -1;
     // Upper bound on units: every sequence adds at most one partial block.
-    const long long bound = static_cast<long long>(Hq) * ((Nq + UNIT_ROWS - 1) / UNIT_ROWS + B);
-    grid = bound < env.sms ? bound : env.sms;
+    const long long bound = static_cast<long long>(Hq) * ((Nq + unit_rows - 1) / unit_rows + B);
+    grid = bound < workers ? bound : workers;
   } else {
-    prm.nqb = (Nq + UNIT_ROWS - 1) / UNIT_ROWS;
+    prm.nqb = (Nq + unit_rows - 1) / unit_rows;
     const long long units = static_cast<long long>(B) * Hq * prm.nqb;
     if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
     prm.num_units = static_cast<int>(units);
-    grid = units < env.sms ? units : env.sms;
+    grid = units < workers ? units : workers;
   }
   if (grid <= 0) return FA_OK;
+  if constexpr (D == 128) {
+    if (pair) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(2 * grid), 1, 1);
+      cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = Cfg<D, false, true>::SMEM_BYTES;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, false, 0, true>, tq, tk, tv, prm) != cudaSuccess)
+        return FA_ERR_CUDA;
+      return FA_OK;
+    }
+  }
   if (soft)
-    fa_fwd_kernel<D, false, SOFT_EXP_PERIOD>
+    fa_fwd_kernel<D, false, SOFT_EXP_PERIOD, false>
         <<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
   else
-    fa_fwd_kernel<D, false, 0><<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+    fa_fwd_kernel<D, false, 0, false>
+        <<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
@@ -953,7 +1138,8 @@ fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const 
   constexpr int D = 128;
   using C = Cfg<D, true>;
   const bool soft = env.soft_exp != 0;
-  if (!(soft ? prepare_kernel<D, true, SOFT_EXP_PERIOD>(env.device) : prepare_kernel<D, true, 0>(env.device)))
+  if (!(soft ? prepare_kernel<D, true, SOFT_EXP_PERIOD, false>(env.device)
+             : prepare_kernel<D, true, 0, false>(env.device)))
     return FA_ERR_CUDA;
   alignas(64) CUtensorMap tq, tk, tv;
   std::memset(&tk, 0, sizeof(tk));
@@ -979,17 +1165,18 @@ fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const 
   prm.q_descale = q_descale;
   prm.k_descale = k_descale;
   prm.v_descale = v_descale;
-  prm.nqb = (Nq + UNIT_ROWS - 1) / UNIT_ROWS;
+  prm.nqb = (Nq + C::UNIT_ROWS - 1) / C::UNIT_ROWS;
   const long long units = static_cast<long long>(B) * Hq * prm.nqb;
   if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
   prm.num_units = static_cast<int>(units);
   const long long grid = units < env.sms ? units : env.sms;
   if (grid <= 0) return FA_OK;
   if (soft)
-    fa_fwd_kernel<D, true, SOFT_EXP_PERIOD><<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM_BYTES, stream>>>(
-        tq, tk, tv, prm);
+    fa_fwd_kernel<D, true, SOFT_EXP_PERIOD, false>
+        <<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
   else
-    fa_fwd_kernel<D, true, 0><<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
+    fa_fwd_kernel<D, true, 0, false>
+        <<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }

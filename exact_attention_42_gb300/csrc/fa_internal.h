@@ -28,6 +28,7 @@ struct LaunchEnv {
   unsigned long long wait_limit_ns = 0;  // bound on every mbarrier wait
   int fault_mode = 0;                   // test hook, see fa_debug_fault_injection
   int soft_exp = 0;                     // test hook, see fa_debug_soft_exp
+  int fwd_pair = 0;                     // test hook, see fa_debug_fwd_pair
 };
 
 // Forward kernel (fa_fwd.cu); dispatches to the split-KV path itself.

@@ -20,9 +20,9 @@
  * Thread safety: every entry point is reentrant.  The library's state is
  * once-initialised per-device launch settings, three device status words (one
  * each for the forward, split-KV and backward kernels, merged by
- * fa_device_status) and the process-wide settings of the two test hooks
- * (fa_debug_fault_injection, fa_debug_soft_exp): a hook call changes every
- * later launch, from any thread.
+ * fa_device_status) and the process-wide settings of the three test hooks
+ * (fa_debug_fault_injection, fa_debug_soft_exp, fa_debug_fwd_pair): a hook
+ * call changes every later launch, from any thread.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H
@@ -247,6 +247,23 @@ fa_status fa_debug_exp2_soft(const float* x, float* y, int n, cudaStream_t strea
  * measured slower on GB300.  FA_ERR_VALUE for other arguments.
  */
 fa_status fa_debug_soft_exp(int on);
+
+/*
+ * fa_debug_fwd_pair -- test hook (process-wide, affects every later fa_fwd
+ * launch of a bf16 problem with d = 128): on = 1 runs the CTA-pair forward
+ * kernel instead of the single-CTA one; on = 0 (the default) restores it.
+ * The pair kernel computes the same O and LSE with tensor-core products
+ * shared by the two CTAs of a cluster (tcgen05 cta_group::2, M = 256: each
+ * CTA holds its own 128 query rows of a product tile, and half of every K
+ * tile (64 keys) and V tile (64 head dims), so a K/V tile is read from L2
+ * once per pair).  The interview canvas's Blackwell notes (element
+ * v4-card-body) name these 2-CTA products.  It is off by default because it
+ * measured slower on GB300: the forward step there is set by the one thread
+ * that issues the products and by each query tile's softmax-then-products
+ * chain, and a pair has one issuing thread for two SMs.  Results stay within
+ * the same tolerances.  FA_ERR_VALUE for other arguments.
+ */
+fa_status fa_debug_fwd_pair(int on);
 
 /* Dynamic shared memory (bytes) and threads per CTA used for head dim d;
  * 0 for an unsupported d.  For tooling and tests. */
