@@ -42,7 +42,7 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd TFLOP/s bf16 (N=4096,d=128,causal) and % of dense-BF16 peak"
 METRIC_BWD = "attention bwd TFLOP/s bf16 (dQ, dK, dV; 2.5x the forward FLOPs) and % of dense-BF16 peak"
-METRIC_FP8 = "attention fwd TFLOP/s fp8 e4m3 (d=128) and % of dense-FP8 peak"
+METRIC_FP8 = "attention fwd TFLOP/s fp8 e4m3 and % of dense-FP8 peak"
 FP8_OVER_BF16 = 2.0   # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s)
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}

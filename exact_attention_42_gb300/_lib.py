@@ -60,7 +60,7 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, ci,
                                  vp, vp]
             L.fa_bwd.restype = ci
-            L.fa_fwd_fp8.argtypes = [vp] * 8 + [ci] * 6 + [ctypes.c_float, ci, vp]
+            L.fa_fwd_fp8.argtypes = [vp] * 8 + [ci] * 6 + [ctypes.c_float, ci, vp, vp]
             L.fa_fwd_fp8.restype = ci
             L.fa_bwd_smem_bytes.argtypes = [ci]
             L.fa_bwd_smem_bytes.restype = ci
@@ -89,10 +89,10 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, delta, B, Hq, Hkv, Nq, Nk, d, scal
 
 
 def fa_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal,
-               stream) -> int:
+               cu_seqlens, stream) -> int:
     """Direct call of the 8-bit forward entry point with integer addresses; returns the status."""
     return lib().fa_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, Nq, Nk, d,
-                            ctypes.c_float(scale), int(causal), stream)
+                            ctypes.c_float(scale), int(causal), cu_seqlens, stream)
 
 
 def fa_fp8_quantize(x, x8, descale, B, H, N, d, transpose, signs, stream) -> int:

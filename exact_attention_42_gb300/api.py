@@ -216,39 +216,56 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
 def fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, vt8: torch.Tensor, q_descale: torch.Tensor,
             k_descale: torch.Tensor, v_descale: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-            stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+            stream: Optional[torch.cuda.Stream] = None,
+            cu_seqlens: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Attention forward with e4m3 inputs on the GPU; returns (O bf16, LSE fp32).
 
-    q8 [B, Hq, Nq, 128], k8 [B, Hkv, Nk, 128] and vt8 [B, Hkv, 128, Nk] hold
-    e4m3 codes (torch.uint8 or torch.float8_e4m3fn); the descales are fp32
-    [B, Hq], [B, Hkv], [B, Hkv].  Nk must be a multiple of 16.
+    Dense: q8 [B, Hq, Nq, d], k8 [B, Hkv, Nk, d] and vt8 [B, Hkv, d, Nk] hold
+    e4m3 codes (torch.uint8 or torch.float8_e4m3fn), d = 64 or 128; the
+    descales are fp32 [B, Hq], [B, Hkv], [B, Hkv].  Nk must be a multiple of 16.
+    Packed (cu_seqlens int32 [nseq+1] on the device): q8 [Hq, T, d],
+    k8 [Hkv, T, d], vt8 [Hkv, d, T] and descales [Hq], [Hkv], [Hkv] (one per
+    head); T must be a multiple of 16.
     """
     dev = q8.device
     as_u8 = lambda t: t.view(torch.uint8) if t.dtype != torch.uint8 else t
     q8, k8, vt8 = as_u8(q8), as_u8(k8), as_u8(vt8)
-    _check(q8, "q8", torch.uint8, 4, None)
-    _check(k8, "k8", torch.uint8, 4, dev)
-    _check(vt8, "vt8", torch.uint8, 4, dev)
-    B, Hq, Nq, d = q8.shape
-    Bk, Hkv, Nk, dk = k8.shape
-    if Bk != B or dk != d or tuple(vt8.shape) != (B, Hkv, d, Nk):
-        raise ValueError("k8 must be [B, Hkv, Nk, d] and vt8 [B, Hkv, d, Nk]")
-    for t, n, shp in ((q_descale, "q_descale", (B, Hq)), (k_descale, "k_descale", (B, Hkv)),
-                      (v_descale, "v_descale", (B, Hkv))):
-        _check(t, n, torch.float32, 2, dev)
+    packed = cu_seqlens is not None
+    nd = 3 if packed else 4
+    _check(q8, "q8", torch.uint8, nd, None)
+    _check(k8, "k8", torch.uint8, nd, dev)
+    _check(vt8, "vt8", torch.uint8, nd, dev)
+    if packed:
+        _check(cu_seqlens, "cu_seqlens", torch.int32, 1, dev)
+        Hq, Nq, d = q8.shape
+        Hkv, Nk, dk = k8.shape
+        B = cu_seqlens.numel() - 1
+        if Nk != Nq or dk != d or tuple(vt8.shape) != (Hkv, d, Nk):
+            raise ValueError("packed k8 must be [Hkv, T, d] and vt8 [Hkv, d, T] with q8's T and d")
+        shapes = ((Hq,), (Hkv,), (Hkv,))
+        row_shape = (Hq, Nq)
+    else:
+        B, Hq, Nq, d = q8.shape
+        Bk, Hkv, Nk, dk = k8.shape
+        if Bk != B or dk != d or tuple(vt8.shape) != (B, Hkv, d, Nk):
+            raise ValueError("k8 must be [B, Hkv, Nk, d] and vt8 [B, Hkv, d, Nk]")
+        shapes = ((B, Hq), (B, Hkv), (B, Hkv))
+        row_shape = (B, Hq, Nq)
+    for t, n, shp in zip((q_descale, k_descale, v_descale), ("q_descale", "k_descale", "v_descale"), shapes):
+        _check(t, n, torch.float32, len(shp), dev)
         if tuple(t.shape) != shp:
             raise ValueError("%s must be %s" % (n, shp))
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
-        out = torch.empty((B, Hq, Nq, d), dtype=torch.bfloat16, device=dev)
+        out = torch.empty(tuple(q8.shape), dtype=torch.bfloat16, device=dev)
     if lse is None:
-        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+        lse = torch.empty(row_shape, dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
         s = stream if stream is not None else torch.cuda.current_stream(dev)
         st = fa_fwd_fp8(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), q_descale.data_ptr(), k_descale.data_ptr(),
                         v_descale.data_ptr(), out.data_ptr(), lse.data_ptr(), B, Hq, Hkv, Nq, Nk, d, float(scale),
-                        int(bool(causal)), s.cuda_stream)
+                        int(bool(causal)), cu_seqlens.data_ptr() if packed else None, s.cuda_stream)
     if st != 0:
         raise FaError(st, "fa_fwd_fp8")
     return out, lse
@@ -313,7 +330,7 @@ def fwd_fp8_from_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal:
                       stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """The 8-bit forward from bf16 inputs: quantizes Q and K (rotated with one
     seeded sign vector when ``rotate``) and V (transposed), then runs
-    ``fwd_fp8``; returns (O bf16, LSE fp32).  d must be 128."""
+    ``fwd_fp8``; returns (O bf16, LSE fp32).  Dense layout, d = 64 or 128."""
     signs = hadamard_signs(q.shape[-1], seed, q.device) if rotate else None
     q8, qd = fp8_quantize(q, signs, stream=stream)
     k8, kd = fp8_quantize(k, signs, stream=stream)

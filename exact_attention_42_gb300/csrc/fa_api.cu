@@ -137,10 +137,11 @@ int fa_decode_smem_bytes(int d) { return fa::decode_smem_bytes(d); }
 
 fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
                      const float* k_descale, const float* v_descale, void* o, float* lse, int B, int Hq, int Hkv,
-                     int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream) {
+                     int Nq, int Nk, int d, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream) {
   if (B < 0 || Hq < 0 || Hkv < 1 || Nq < 0 || Nk < 0) return FA_ERR_SHAPE;
   if (Hq % Hkv != 0) return FA_ERR_SHAPE;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (cu_seqlens != nullptr && Nq != Nk) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (Nk % 16 != 0) return FA_ERR_SHAPE;  // rows of V^T are Nk bytes: a multiple of 16
   if (!(std::isfinite(scale) && scale > 0.f)) return FA_ERR_VALUE;
   if (B == 0 || Hq == 0 || Nq == 0) return FA_OK;
@@ -150,12 +151,13 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
   auto mis = [](const void* ptr, unsigned a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) != 0; };
   if (mis(q8, 16) || mis(o, 16) || (Nk > 0 && (mis(k8, 16) || mis(vt8, 16)))) return FA_ERR_ALIGN;
   if (mis(lse, 4) || mis(q_descale, 4) || (Nk > 0 && (mis(k_descale, 4) || mis(v_descale, 4)))) return FA_ERR_ALIGN;
-  if (static_cast<long long>(B) * Hq > 0x7fffffffLL) return FA_ERR_SHAPE;
+  if (cu_seqlens != nullptr && mis(cu_seqlens, 4)) return FA_ERR_ALIGN;
+  if (cu_seqlens == nullptr && static_cast<long long>(B) * Hq > 0x7fffffffLL) return FA_ERR_SHAPE;
   fa::LaunchEnv env;
   const fa_status st = fa::launch_env(&env);
   if (st != FA_OK) return st;
-  return fa::launch_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal,
-                            stream, env);
+  return fa::launch_fwd_fp8(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, Nq, Nk, d, scale,
+                            causal, cu_seqlens, stream, env);
 }
 
 fa_status fa_fp8_quantize(const void* x, void* x8, float* descale, int B, int H, int N, int d, int transpose,

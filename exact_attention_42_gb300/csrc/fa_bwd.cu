@@ -191,6 +191,8 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const __nv_bfloat16* __r
                                                         const __nv_bfloat16* __restrict__ dout,
                                                         float* __restrict__ delta, long long rows) {
   constexpr int TPR = D / 8;
+  grid_dependency_wait();  // O and dO may come from the previous kernel in the stream
+  if (threadIdx.x == 0) grid_launch_dependents();
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long row = t / TPR;
   const int part = static_cast<int>(t % TPR);
@@ -369,6 +371,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Set-up above overlaps the previous kernel's tail; global memory only after it.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_tiles(p) * (KV_KERNEL ? p.Hkv : p.Hq);
   const int nrounds = (num_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
 
@@ -762,6 +767,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Set-up above overlaps the previous kernel's tail; global memory only after it.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_tiles(p) * (KV_KERNEL ? p.Hkv : p.Hq);
   const int nrounds = (num_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
 
@@ -1140,9 +1148,10 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
     const long long threads = rows * (D / 8);
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return FA_ERR_SHAPE;
-    bwd::bwd_delta_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), delta, rows);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    PdlLaunch L(dim3(static_cast<unsigned>(blocks)), 256, 0, stream);
+    if (cudaLaunchKernelEx(&L.cfg, bwd::bwd_delta_kernel<D>, static_cast<const __nv_bfloat16*>(o),
+                           static_cast<const __nv_bfloat16*>(dout), delta, rows) != cudaSuccess)
+      return FA_ERR_CUDA;
   }
   alignas(64) CUtensorMap tq, tdo, tk, tv;
   std::memset(&tk, 0, sizeof(tk));
@@ -1186,9 +1195,8 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
     prm.fault_inject = fault_mode == kFaultBwdDq ? 1 : 0;
     const long long grid = units < sms ? units : sms;
     if (grid > 0) {
-      bwd::bwd_dq_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, CQ::SMEM_BYTES, stream>>>(tq, tdo, tk,
-                                                                                                        tv, prm);
-      if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+      PdlLaunch L(dim3(static_cast<unsigned>(grid)), bwd::NUM_THREADS, CQ::SMEM_BYTES, stream);
+      if (cudaLaunchKernelEx(&L.cfg, bwd::bwd_dq_kernel<D>, tq, tdo, tk, tv, prm) != cudaSuccess) return FA_ERR_CUDA;
     }
   }
   // dK, dV: one unit per (batch or sequence, key/value head, key tile).
@@ -1199,9 +1207,8 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
     prm.fault_inject = fault_mode == kFaultBwdDkdv ? 1 : 0;
     const long long grid = units < sms ? units : sms;
     if (grid > 0) {
-      bwd::bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid), bwd::NUM_THREADS, CKV::SMEM_BYTES, stream>>>(
-          tq, tdo, tk, tv, prm);
-      if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+      PdlLaunch L(dim3(static_cast<unsigned>(grid)), bwd::NUM_THREADS, CKV::SMEM_BYTES, stream);
+      if (cudaLaunchKernelEx(&L.cfg, bwd::bwd_dkdv_kernel<D>, tq, tdo, tk, tv, prm) != cudaSuccess) return FA_ERR_CUDA;
     }
   }
   return FA_OK;

@@ -169,6 +169,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  // Set-up above overlaps the previous kernel's tail; global memory only after it.
+  grid_dependency_wait();
+  if (tid == 0) grid_launch_dependents();
 
   // Online-softmax state of a compute warp for fragment rows g and g + 8
   // (g = lane / 4): reference max m, partial sum l, output fragments o.
@@ -491,19 +494,12 @@ static fa_status launch_decode_t(const void* q, const void* k, const void* v, vo
   prm.wait_limit_ns = wait_limit_ns;
   prm.fault_inject = fault_mode == kFaultDecode ? 1 : 0;
 
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(S), static_cast<unsigned>(groups), 1);
-  cfg.blockDim = dim3(dec::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = dec::Cfg<D>::SMEM_BYTES;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(S);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, dec::decode_kernel<D>, tk, tv, prm) != cudaSuccess) return FA_ERR_CUDA;
+  // One cluster of S CTAs per (batch, key/value head); clusters of one CTA are
+  // still launched as clusters so that the split merge code is the same.
+  PdlLaunch L(dim3(static_cast<unsigned>(S), static_cast<unsigned>(groups), 1), dec::THREADS,
+              dec::Cfg<D>::SMEM_BYTES, stream, static_cast<unsigned>(S));
+  L.cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&L.cfg, dec::decode_kernel<D>, tk, tv, prm) != cudaSuccess) return FA_ERR_CUDA;
   return FA_OK;
 }
 

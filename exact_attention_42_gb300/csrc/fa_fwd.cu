@@ -127,15 +127,19 @@ __device__ int g_fa_status;
 template <int D, bool FP8 = false, bool PAIR = false>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static_assert(!FP8 || D == 128, "the 8-bit path is built for d = 128");
   static_assert(!PAIR || (D == 128 && !FP8), "the CTA-pair path is built for bf16, d = 128");
   static constexpr int ELEM = FP8 ? 1 : 2;             // bytes per element
-  static constexpr int TILE_BYTES = BLOCK_M * D * ELEM;  // one 128 x D tile
-  static constexpr int CHUNKS = D * ELEM / 128;        // 128-byte swizzle column blocks
+  static constexpr int TILE_BYTES = BLOCK_M * D * ELEM;  // one 128 x D tile (a V^T tile, D x 128 keys, likewise)
+  // Q and K rows are D * ELEM bytes: 128-byte swizzle column blocks, except
+  // the 8-bit d = 64 rows of 64 bytes, which use the 64-byte swizzle.
+  static constexpr int ROW_BYTES = D * ELEM;
+  static constexpr bool SW64 = ROW_BYTES == 64;
+  static constexpr int CHUNKS = SW64 ? 1 : ROW_BYTES / 128;  // swizzle column blocks per Q/K row
   static constexpr int CHUNK_COLS = 128 / ELEM;        // elements per column block
   static constexpr int CHUNK_BYTES = BLOCK_M * 128;    // 16 KB
+  static constexpr int QK_SBO = SW64 ? 512 : 1024;     // bytes between 8-row groups of a Q/K tile
   static constexpr int SLOT_BYTES = PAIR ? TILE_BYTES / 2 : TILE_BYTES;  // a pair's CTA holds half a tile
-  static constexpr int NS = PAIR ? 10 : ((TILE_BYTES == 32768) ? 5 : 8);  // K/V ring slots
+  static constexpr int NS = PAIR ? 10 : (TILE_BYTES == 32768 ? 5 : (TILE_BYTES == 16384 ? 8 : 16));  // ring slots
   static constexpr int QK_KSTEPS = D * ELEM / 32;      // 32 bytes of K per product
   static constexpr int PV_KSTEPS = BLOCK_N * ELEM / 32;
   static constexpr int SMEM_Q = NQT * TILE_BYTES;
@@ -160,6 +164,7 @@ struct Params {
   int num_units;          // dense: B * Hq * nqb; packed: computed on the device
   unsigned long long wait_limit_ns;  // bound on every mbarrier wait
   int fault_inject;       // test hook: 1 = the K/V producer withholds its first fill
+  int key_align;          // packed sequences: key tiles start at a multiple of this many tokens (1 or 16)
   // 8-bit path only: per-(batch, head) descale factors of Q [B*Hq], K and V
   // [B*Hkv]; the real inputs are code * descale.
   const float* q_descale;
@@ -170,7 +175,8 @@ struct Params {
 struct Unit {
   int Lq, Lk;        // sequence lengths (queries, keys)
   int row0;          // first query row of the unit, local to the sequence
-  int q_y, k_y;      // TMA row coordinate of the sequence's first token
+  int q_y, k_y;      // TMA row coordinate of the sequence's first token (keys: minus kshift)
+  int kshift;        // key tiles start kshift keys before the sequence (8-bit packed path: k_y % 16 == 0)
   int q_z, k_z;      // TMA head coordinate
   long long out_row; // global row index (in O / LSE rows) of the sequence's token 0
 };
@@ -191,6 +197,7 @@ __device__ __forceinline__ bool decode_unit(const Params& p, int u, Unit& w, int
     w.row0 = qb * unit_rows;
     w.q_y = 0;
     w.k_y = 0;
+    w.kshift = 0;
     w.q_z = bh;
     w.k_z = b * p.Hkv + h / p.group;
     w.out_row = static_cast<long long>(bh) * p.Nq;
@@ -211,7 +218,12 @@ __device__ __forceinline__ bool decode_unit(const Params& p, int u, Unit& w, int
       w.Lk = L;
       w.row0 = (nb - 1 - blk) * unit_rows;
       w.q_y = prev;
-      w.k_y = prev;
+      // The 8-bit path reads V^T tiles along the token axis, where a TMA box
+      // must start on a 16-byte boundary: its key tiles start at the multiple
+      // of 16 at or below the sequence start, and the keys before the start
+      // are masked.
+      w.kshift = prev % p.key_align;
+      w.k_y = prev - w.kshift;
       w.q_z = h;
       w.k_z = h / p.group;
       w.out_row = static_cast<long long>(h) * T + prev;
@@ -246,7 +258,7 @@ __device__ __forceinline__ int kv_tiles(const Params& p, const Unit& w, int t, i
     last_key = min(last_key, last_row + (w.Lk - w.Lq));
     if (last_key < 0) return 0;
   }
-  return last_key / BLOCK_N + 1;
+  return (last_key + w.kshift) / BLOCK_N + 1;
 }
 
 // Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0),
@@ -392,6 +404,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, PAIR ? cluster_addr(smem_u32(const_cast<int*>(abort_flag)), rank ^ 1u) : 0u, PAIR};
+  // Everything above touches only this CTA's shared memory and TMEM, so it
+  // overlaps the tail of the previous kernel in the stream; inputs (including
+  // cu_seqlens) and outputs are touched only after that kernel is done.  The
+  // next kernel may then start its own set-up on the SMs this grid frees.
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
 
   const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_num_units(p, C::UNIT_ROWS);
   // Static "snake" schedule over the grid's G persistent workers (CTAs, or
@@ -555,9 +573,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // 128-row tile, or the 64-key half a CTA of a pair holds.
     constexpr int K_CHUNK_BYTES = C::SLOT_BYTES / C::CHUNKS;
     // S_t = Q_t K^T: both operands K-major (head dim contiguous), 16 columns per MMA.
+    auto qk_desc = [&](uint32_t addr) {
+      return C::SW64 ? smem_desc_sw64(addr, 16, C::QK_SBO) : smem_desc_sw128(addr, 16, C::QK_SBO);
+    };
     auto issue_qk = [&](int t, int slot) {
-      const uint64_t q_desc = smem_desc_sw128(q_addr + t * C::TILE_BYTES, 16, 1024);
-      const uint64_t k_desc = smem_desc_sw128(ring_addr + slot * C::SLOT_BYTES, 16, 1024);
+      const uint64_t q_desc = qk_desc(q_addr + t * C::TILE_BYTES);
+      const uint64_t k_desc = qk_desc(ring_addr + slot * C::SLOT_BYTES);
 #pragma unroll
       for (int kk = 0; kk < C::QK_KSTEPS; ++kk) {
         const uint64_t qoff = static_cast<uint64_t>((kk / 4) * C::CHUNK_BYTES + (kk % 4) * 32) >> 4;
@@ -761,8 +782,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < BLOCK_N; ++i) s[i] = __uint_as_float(raw[i]);
         }
-        const int k0 = j * BLOCK_N;
-        const bool need_mask = (k0 + BLOCK_N > w.Lk) || (p.causal && k0 + BLOCK_N - 1 > tile_diag);
+        // Key of column 0; on the 8-bit packed path the first tile of a
+        // sequence starts up to 15 keys early (columns of the previous sequence).
+        const int k0 = j * BLOCK_N - (FP8 ? w.kshift : 0);
+        const bool need_mask = (FP8 && k0 < 0) || (k0 + BLOCK_N > w.Lk) || (p.causal && k0 + BLOCK_N - 1 > tile_diag);
         // Column c of this row is visible iff c <= rel (one compare against a
         // constant per element).  rel_hi, the warp's largest limit, lets the
         // exponential loop below skip 32-column chunks no lane can see.
@@ -774,6 +797,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int c = 0; c < BLOCK_N; ++c)
             if (c > rel) s[c] = NEG_INF;
+          if constexpr (FP8) {
+#pragma unroll
+            for (int c = 0; c < BLOCK_N; ++c)
+              if (c < -k0) s[c] = NEG_INF;
+          }
         }
         // Row max: 3-input max in 4 independent chains.
         float mx4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
@@ -1015,6 +1043,15 @@ static bool prepare_kernel(int device, int* pairs = nullptr) {
   return true;
 }
 
+// Launches one instantiation on `stream` (programmatic stream serialization,
+// see PdlLaunch) as `clusters` clusters of `cta_per` CTAs.
+template <typename Kernel>
+static fa_status launch_kernel(Kernel kernel, long long clusters, int cta_per, int smem, cudaStream_t stream,
+                               const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const Params& prm) {
+  PdlLaunch L(dim3(static_cast<unsigned>(clusters * cta_per)), NUM_THREADS, smem, stream, static_cast<unsigned>(cta_per));
+  return cudaLaunchKernelEx(&L.cfg, kernel, tq, tk, tv, prm) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
 template <int D>
 static fa_status launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                         int Nq, int Nk, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream,
@@ -1066,6 +1103,7 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
   prm.causal = causal ? 1 : 0;
   prm.wait_limit_ns = env.wait_limit_ns;
   prm.fault_inject = env.fault_mode == kFaultFwd ? 1 : 0;
+  prm.key_align = 1;
   prm.q_descale = prm.k_descale = prm.v_descale = nullptr;
   long long grid;  // persistent workers: CTAs, or CTA pairs
   if (packed) {
@@ -1083,32 +1121,14 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
   }
   if (grid <= 0) return FA_OK;
   if constexpr (D == 128) {
-    if (pair) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>(2 * grid), 1, 1);
-      cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-      cfg.dynamicSmemBytes = Cfg<D, false, true>::SMEM_BYTES;
-      cfg.stream = stream;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (cudaLaunchKernelEx(&cfg, fa_fwd_kernel<D, false, 0, true>, tq, tk, tv, prm) != cudaSuccess)
-        return FA_ERR_CUDA;
-      return FA_OK;
-    }
+    if (pair)
+      return launch_kernel(fa_fwd_kernel<D, false, 0, true>, grid, 2, Cfg<D, false, true>::SMEM_BYTES, stream, tq,
+                           tk, tv, prm);
   }
   if (soft)
-    fa_fwd_kernel<D, false, SOFT_EXP_PERIOD, false>
-        <<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
-  else
-    fa_fwd_kernel<D, false, 0, false>
-        <<<static_cast<unsigned>(grid), NUM_THREADS, Cfg<D>::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  return FA_OK;
+    return launch_kernel(fa_fwd_kernel<D, false, SOFT_EXP_PERIOD, false>, grid, 1, Cfg<D>::SMEM_BYTES, stream, tq, tk,
+                         tv, prm);
+  return launch_kernel(fa_fwd_kernel<D, false, 0, false>, grid, 1, Cfg<D>::SMEM_BYTES, stream, tq, tk, tv, prm);
 }
 
 fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
@@ -1118,40 +1138,47 @@ fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float
   return launch<64>(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal, cu_seqlens, stream, env);
 }
 
-// [heads, rows, cols] uint8 tensor read in 128-row x 128-byte boxes with the
-// 128-byte swizzle (the K-major layout of an 8-bit operand tile).
-static bool encode_u8_map(CUtensorMap* map, const void* base, long long cols, long long rows, long long heads) {
+// [heads, rows, cols] uint8 tensor read in box_rows x box_cols boxes with the
+// 128-byte swizzle (box_cols = 128) or the 64-byte swizzle (box_cols = 64):
+// the K-major layout of an 8-bit operand tile.
+static bool encode_u8_map(CUtensorMap* map, const void* base, long long cols, long long rows, long long heads,
+                          int box_cols, int box_rows) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(heads)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows * cols)};
-  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(BLOCK_M), 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t elem[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, elem,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+             CU_TENSOR_MAP_INTERLEAVE_NONE, box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
-                         const float* k_descale, const float* v_descale, void* o, float* lse, int B, int Hq, int Hkv,
-                         int Nq, int Nk, float scale, int causal, cudaStream_t stream, const LaunchEnv& env) {
-  constexpr int D = 128;
+template <int D>
+static fa_status launch_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
+                            const float* k_descale, const float* v_descale, void* o, float* lse, int B, int Hq,
+                            int Hkv, int Nq, int Nk, float scale, int causal, const int32_t* cu_seqlens,
+                            cudaStream_t stream, const LaunchEnv& env) {
   using C = Cfg<D, true>;
   const bool soft = env.soft_exp != 0;
   if (!(soft ? prepare_kernel<D, true, SOFT_EXP_PERIOD, false>(env.device)
              : prepare_kernel<D, true, 0, false>(env.device)))
     return FA_ERR_CUDA;
+  const bool packed = cu_seqlens != nullptr;
+  const long long q_heads = packed ? Hq : static_cast<long long>(B) * Hq;
+  const long long kv_heads = packed ? Hkv : static_cast<long long>(B) * Hkv;
   alignas(64) CUtensorMap tq, tk, tv;
   std::memset(&tk, 0, sizeof(tk));
   std::memset(&tv, 0, sizeof(tv));
-  if (!encode_u8_map(&tq, q8, D, Nq, static_cast<long long>(B) * Hq)) return FA_ERR_CUDA;
-  if (Nk > 0 && (!encode_u8_map(&tk, k8, D, Nk, static_cast<long long>(B) * Hkv) ||
-                 !encode_u8_map(&tv, vt8, Nk, D, static_cast<long long>(B) * Hkv)))
+  // Q and K: rows of D bytes (one swizzle block); V^T: D rows of Nk bytes, read in 128-key boxes.
+  if (!encode_u8_map(&tq, q8, D, Nq, q_heads, C::ROW_BYTES, BLOCK_M)) return FA_ERR_CUDA;
+  if (Nk > 0 && (!encode_u8_map(&tk, k8, D, Nk, kv_heads, C::ROW_BYTES, BLOCK_M) ||
+                 !encode_u8_map(&tv, vt8, Nk, D, kv_heads, BLOCK_N, D)))
     return FA_ERR_CUDA;
   Params prm;
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
-  prm.cu_seqlens = nullptr;
+  prm.cu_seqlens = cu_seqlens;
   prm.B = B;
   prm.Hq = Hq;
   prm.Hkv = Hkv;
@@ -1162,23 +1189,39 @@ fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const 
   prm.causal = causal ? 1 : 0;
   prm.wait_limit_ns = env.wait_limit_ns;
   prm.fault_inject = 0;
+  prm.key_align = packed ? 16 : 1;  // V^T boxes start on 16-byte (16-key) boundaries
   prm.q_descale = q_descale;
   prm.k_descale = k_descale;
   prm.v_descale = v_descale;
-  prm.nqb = (Nq + C::UNIT_ROWS - 1) / C::UNIT_ROWS;
-  const long long units = static_cast<long long>(B) * Hq * prm.nqb;
-  if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
-  prm.num_units = static_cast<int>(units);
-  const long long grid = units < env.sms ? units : env.sms;
+  long long grid;
+  if (packed) {
+    prm.nqb = 0;
+    prm.num_units = -1;
+    const long long bound = static_cast<long long>(Hq) * ((Nq + C::UNIT_ROWS - 1) / C::UNIT_ROWS + B);
+    grid = bound < env.sms ? bound : env.sms;
+  } else {
+    prm.nqb = (Nq + C::UNIT_ROWS - 1) / C::UNIT_ROWS;
+    const long long units = static_cast<long long>(B) * Hq * prm.nqb;
+    if (units > 0x7fffffffLL) return FA_ERR_SHAPE;
+    prm.num_units = static_cast<int>(units);
+    grid = units < env.sms ? units : env.sms;
+  }
   if (grid <= 0) return FA_OK;
   if (soft)
-    fa_fwd_kernel<D, true, SOFT_EXP_PERIOD, false>
-        <<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
-  else
-    fa_fwd_kernel<D, true, 0, false>
-        <<<static_cast<unsigned>(grid), NUM_THREADS, C::SMEM_BYTES, stream>>>(tq, tk, tv, prm);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-  return FA_OK;
+    return launch_kernel(fa_fwd_kernel<D, true, SOFT_EXP_PERIOD, false>, grid, 1, C::SMEM_BYTES, stream, tq, tk, tv,
+                         prm);
+  return launch_kernel(fa_fwd_kernel<D, true, 0, false>, grid, 1, C::SMEM_BYTES, stream, tq, tk, tv, prm);
+}
+
+fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
+                         const float* k_descale, const float* v_descale, void* o, float* lse, int B, int Hq, int Hkv,
+                         int Nq, int Nk, int d, float scale, int causal, const int32_t* cu_seqlens,
+                         cudaStream_t stream, const LaunchEnv& env) {
+  if (d == 64)
+    return launch_fp8<64>(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal,
+                          cu_seqlens, stream, env);
+  return launch_fp8<128>(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal,
+                         cu_seqlens, stream, env);
 }
 
 int fwd_status_and_clear() {

@@ -21,6 +21,33 @@ constexpr int kFaultBwdDq = 3;   // bwd_dq_kernel's K/V producer
 constexpr int kFaultBwdDkdv = 4; // bwd_dkdv_kernel's Q/dO producer
 constexpr int kFaultModes = 5;
 
+// Launch configuration with programmatic stream serialization: the kernel
+// may start before the previous kernel in `stream` has finished, runs its
+// shared-memory and TMEM set-up meanwhile, and waits for that kernel
+// (griddepcontrol.wait) before it touches global memory.  cluster_x > 1
+// launches clusters of that many CTAs.  cfg points into this object, so it
+// is used in place: PdlLaunch L(...); cudaLaunchKernelEx(&L.cfg, ...).
+struct PdlLaunch {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[2];
+  PdlLaunch(dim3 grid, unsigned threads, size_t smem, cudaStream_t stream, unsigned cluster_x = 1) {
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cluster_x > 1 ? 2 : 1;
+  }
+  PdlLaunch(const PdlLaunch&) = delete;
+  PdlLaunch& operator=(const PdlLaunch&) = delete;
+};
+
 // Per-call launch settings resolved by the entry points (fa_api.cu).
 struct LaunchEnv {
   int device = 0;
@@ -35,11 +62,12 @@ struct LaunchEnv {
 fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                      int Nq, int Nk, int d, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream,
                      const LaunchEnv& env);
-// 8-bit forward (fa_fwd.cu, d = 128, dense): e4m3 Q, K and V^T with
-// per-(batch, head) descales.
+// 8-bit forward (fa_fwd.cu, d = 64 or 128, dense or packed): e4m3 Q, K and
+// V^T with per-(batch, head) descales (per head when packed).
 fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
                          const float* k_descale, const float* v_descale, void* o, float* lse, int B, int Hq, int Hkv,
-                         int Nq, int Nk, float scale, int causal, cudaStream_t stream, const LaunchEnv& env);
+                         int Nq, int Nk, int d, float scale, int causal, const int32_t* cu_seqlens,
+                         cudaStream_t stream, const LaunchEnv& env);
 int fwd_status_and_clear();  // -1 if the status word cannot be read
 // e4m3 codes and per-(batch, head) descales of a bf16 tensor (fa_quant.cu).
 fa_status launch_fp8_quantize(const void* x, void* x8, float* descale, int B, int H, int N, int d, int transpose,

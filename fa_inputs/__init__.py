@@ -167,23 +167,30 @@ def f64_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
 
 @dataclasses.dataclass
 class Fp8Problem:
-    """A dense problem quantized to e4m3 with one scale per (batch, head).
+    """A problem quantized to e4m3 with one scale per (batch, head) slice.
 
-    q8 [B, Hq, Nq, d], k8 [B, Hkv, Nk, d] and vt8 [B, Hkv, d, Nk] (V
-    transposed) are e4m3 codes; the real inputs are q8 * q_scale[b, h] and so
-    on.  Each scale is the tensor slice's max |x| / 448 (1 for an all-zero
-    slice), so the slice uses the whole e4m3 range.
+    Dense: q8 [B, Hq, Nq, d], k8 [B, Hkv, Nk, d] and vt8 [B, Hkv, d, Nk] (V
+    transposed) are e4m3 codes, and the real inputs are q8 * q_scale[b, h] and
+    so on, with scales [B, H].  Packed: q8 [Hq, T, d], k8 [Hkv, T, d],
+    vt8 [Hkv, d, T] and scales [H]: the packed tensor counts as one batch.
+    Each scale is the slice's max |x| / 448 (1 for an all-zero slice), so the
+    slice uses the whole e4m3 range.
     """
     base: "Problem"
     q8: np.ndarray
     k8: np.ndarray
     vt8: np.ndarray
-    q_scale: np.ndarray  # [B, Hq] float32
+    q_scale: np.ndarray  # [B, Hq] float32 ([Hq] when packed)
     k_scale: np.ndarray  # [B, Hkv] float32
     v_scale: np.ndarray  # [B, Hkv] float32
 
     def dequantized(self):
-        """(q, k, v) as float64 arrays in the dense layout."""
+        """(q, k, v) as float64 arrays in the problem's layout."""
+        if self.q8.ndim == 3:
+            q = e4m3_bits_to_f64(self.q8) * self.q_scale.astype(np.float64)[:, None, None]
+            k = e4m3_bits_to_f64(self.k8) * self.k_scale.astype(np.float64)[:, None, None]
+            vt = e4m3_bits_to_f64(self.vt8) * self.v_scale.astype(np.float64)[:, None, None]
+            return q, k, np.swapaxes(vt, 1, 2)
         q = e4m3_bits_to_f64(self.q8) * self.q_scale.astype(np.float64)[:, :, None, None]
         k = e4m3_bits_to_f64(self.k8) * self.k_scale.astype(np.float64)[:, :, None, None]
         vt = e4m3_bits_to_f64(self.vt8) * self.v_scale.astype(np.float64)[:, :, None, None]
@@ -199,13 +206,18 @@ def _quantize_slices(x: np.ndarray):
 
 
 def make_fp8(prob: "Problem") -> Fp8Problem:
-    """Quantizes a dense bf16 problem's Q, K, V to e4m3 (V also transposed)."""
-    assert prob.cu_seqlens is None, "the 8-bit path takes dense problems"
+    """Quantizes a bf16 problem's Q, K, V to e4m3 (V also transposed); a
+    packed problem is quantized as one batch (one scale per head)."""
     q, k, v = (bf16_bits_to_f64(x) for x in (prob.q, prob.k, prob.v))
+    packed = prob.cu_seqlens is not None
+    if packed:
+        q, k, v = q[None], k[None], v[None]
     q8, qs = _quantize_slices(q)
     k8, ks = _quantize_slices(k)
     v8, vs = _quantize_slices(v)
     vt8 = np.ascontiguousarray(np.swapaxes(v8, 2, 3))
+    if packed:
+        return Fp8Problem(prob, q8[0], k8[0], vt8[0], qs[0], ks[0], vs[0])
     return Fp8Problem(prob, q8, k8, vt8, qs, ks, vs)
 
 

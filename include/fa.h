@@ -134,27 +134,35 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const int32_t* cu_seqlens, cudaStream_t stream);
 
 /*
- * fa_fwd_fp8 -- the attention forward with 8-bit (e4m3) inputs (dense
- * layout, d = 128 only), on `stream`.  It computes O and LSE of
+ * fa_fwd_fp8 -- the attention forward with 8-bit (e4m3) inputs, on `stream`.
+ * It computes O and LSE of
  *   S = scale * (q8 * q_descale) (k8 * k_descale)^T,  O = softmax(S) (v * v_descale)
  * on the tensor cores' 8-bit path ("FlashAttention v3 Hopper asynchrony"
- * canvas: FP8 is its third technique; per-block descale factors here are
- * per (batch, head)).  P is rounded to e4m3 before the P V product (relative
- * error at most 2^-4 per term); all accumulation is fp32.
- *   q8   [B, Hq,  Nq, 128] e4m3 codes      q_descale [B, Hq]  fp32
- *   k8   [B, Hkv, Nk, 128] e4m3 codes      k_descale [B, Hkv] fp32
- *   vt8  [B, Hkv, 128, Nk] e4m3 codes (V transposed: every operand of the
+ * canvas: FP8 is its third technique; the descale factors here are one per
+ * (batch, head) slice).  P is rounded to e4m3 before the P V product
+ * (relative error at most 2^-4 per term); all accumulation is fp32.
+ * Dense mode (cu_seqlens == NULL), d = 64 or 128:
+ *   q8   [B, Hq,  Nq, d] e4m3 codes        q_descale [B, Hq]  fp32
+ *   k8   [B, Hkv, Nk, d] e4m3 codes        k_descale [B, Hkv] fp32
+ *   vt8  [B, Hkv, d, Nk] e4m3 codes (V transposed: every operand of the
  *        8-bit products is K-major)        v_descale [B, Hkv] fp32
- *   o    [B, Hq, Nq, 128] bf16,  lse [B, Hq, Nq] fp32 (natural log, of S).
- * Nk must be a multiple of 16 (each V^T row is Nk bytes), else FA_ERR_SHAPE;
- * d != 128 gives FA_ERR_UNSUPPORTED.  Masks, conventions, ownership and the
- * other errors are as for fa_fwd (16-byte alignment for q8, k8, vt8 and o,
- * 4 bytes for lse and the descales).
+ *   o    [B, Hq, Nq, d] bf16,  lse [B, Hq, Nq] fp32 (natural log, of S).
+ * Packed mode (cu_seqlens != NULL, as for fa_fwd; Nq == Nk == T tokens):
+ *   q8 [Hq, T, d], k8 [Hkv, T, d], vt8 [Hkv, d, T], o [Hq, T, d], lse [Hq, T],
+ *   and one descale per head: q_descale [Hq], k_descale and v_descale [Hkv]
+ *   (the packed tensor is one batch).  The kernel reads each sequence's keys
+ *   from the multiple of 16 at or below its start, as a TMA box on the token
+ *   axis of vt8 must start on a 16-byte boundary, and masks the keys before
+ *   the start; any offsets work.
+ * Nk (T when packed) must be a multiple of 16 (each V^T row is Nk bytes),
+ * else FA_ERR_SHAPE; other d give FA_ERR_UNSUPPORTED.  Masks, conventions,
+ * ownership and the other errors are as for fa_fwd (16-byte alignment for
+ * q8, k8, vt8 and o, 4 bytes for lse, cu_seqlens and the descales).
  */
 fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
                      const float* k_descale, const float* v_descale, void* o, float* lse,
                      int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
-                     cudaStream_t stream);
+                     const int32_t* cu_seqlens, cudaStream_t stream);
 
 /*
  * fa_fp8_quantize -- e4m3 codes and per-(batch, head) descales of one bf16

@@ -207,3 +207,42 @@ def test_software_exp2_error_bound(fa, dev):
     fa.fa_debug_exp2_soft(z.data_ptr(), w.data_ptr(), 3, torch.cuda.current_stream(dev).cuda_stream)
     torch.cuda.synchronize(dev)
     assert bool(((w > 0) & (w < 1e-37)).all())
+
+
+def test_dependent_calls_in_one_stream(fa, dev):
+    """Each launch may start before the previous kernel in its stream has
+    finished and must wait for it before touching global memory: a chain of
+    calls that read one another's outputs, issued back to back, gives
+    bitwise the same results as the same chain with a synchronisation after
+    every call (the kernels are deterministic)."""
+    prob = make_dense(2, 8, 8, 2048, 2048, 128, seed=31, causal=True)
+    q, k, v = (to_dev(x, dev) for x in (prob.q, prob.k, prob.v))
+    small = make_dense(1, 2, 2, 300, 300, 64, seed=32, causal=False)
+    qs, ks, vs = (to_dev(x, dev) for x in (small.q, small.k, small.v))
+
+    def chain(sync):
+        outs = []
+        o1, l1 = fa.fwd(q, k, v, causal=True)
+        outs += [o1, l1]
+        if sync:
+            torch.cuda.synchronize(dev)
+        o2, l2 = fa.fwd(o1, k, v, causal=True)           # reads the first call's O as queries
+        outs += [o2, l2]
+        if sync:
+            torch.cuda.synchronize(dev)
+        o3, l3 = fa.fwd(qs, ks, vs)                        # a short launch between long ones
+        outs += [o3, l3]
+        o4, l4 = fa.fwd(q, o2, o1, causal=False)          # reads both earlier outputs as K and V
+        outs += [o4, l4]
+        if sync:
+            torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(dev)
+        return outs
+
+    a = chain(False)
+    b = chain(True)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    ref_o, ref_lse = oracle_full(prob)
+    compare(a[0].float().cpu().numpy().astype(np.float64), a[1].cpu().numpy().astype(np.float64), ref_o, ref_lse,
+            "first call of the chain")

@@ -17,7 +17,7 @@ import numpy as np
 import pytest
 import torch
 
-from fa_inputs import make_dense, make_fp8, make_workload
+from fa_inputs import make_dense, make_fp8, make_varlen, make_workload
 from fa_testutil import LSE_RTOL
 from oracle import attention_fwd
 
@@ -118,3 +118,84 @@ def test_fp8_headline_full_size(fa, dev):
             bound, _ = attention_fwd(qs, ks, np.abs(vs), p.scale, True)
             _check(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], ref_o, ref_lse, bound,
                    "fp8 headline b=%d h=%d" % (b, h))
+
+
+FP8_D64 = [
+    # (B, Hq, Hkv, Nq, Nk, causal); d = 64 (rows of 64 bytes: the 64-byte swizzle)
+    (1, 2, 2, 128, 128, False),
+    (1, 4, 2, 200, 256, False),
+    (2, 4, 2, 300, 304, True),
+    (1, 2, 2, 400, 208, True),
+    (1, 8, 1, 640, 640, True),
+]
+
+
+@pytest.mark.parametrize("shape", FP8_D64, ids=["d64-" + "-".join(map(str, s)) for s in FP8_D64])
+def test_fp8_d64_matches_oracle(fa, dev, shape):
+    B, Hq, Hkv, Nq, Nk, causal = shape
+    p = make_dense(B, Hq, Hkv, Nq, Nk, 64, seed=sum(shape) + 700, causal=causal, name="fp8 d64")
+    f8 = make_fp8(p)
+    o, lse = _run(fa, f8, dev)
+    q, k, v = f8.dequantized()
+    ref_o, ref_lse = attention_fwd(q, k, v, p.scale, causal)
+    bound, _ = attention_fwd(q, k, np.abs(v), p.scale, causal)
+    _check(o, lse, ref_o, ref_lse, bound, "fp8 d64 %s" % (shape,))
+
+
+def _run_packed(fa, f8, dev):
+    u8 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+    p = f8.base
+    cu = torch.from_numpy(p.cu_seqlens).to(dev)
+    o, lse = fa.fwd_fp8(u8(f8.q8), u8(f8.k8), u8(f8.vt8), f32(f8.q_scale), f32(f8.k_scale), f32(f8.v_scale),
+                        causal=p.causal, scale=p.scale, cu_seqlens=cu)
+    torch.cuda.synchronize(dev)
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+# Sequence starts that are not multiples of 16 tokens: the kernel reads each
+# sequence's key tiles from the multiple of 16 below its start and masks the
+# keys before it.  Every total is a multiple of 16 (rows of V^T are T bytes).
+FP8_PACKED = [
+    ([1, 127, 128, 129, 0, 300, 256, 700, 7], 4, 2, 128, True),
+    ([1, 127, 128, 129, 0, 300, 256, 700, 7], 4, 2, 128, False),
+    ([17, 5, 513, 3, 1000, 14], 2, 2, 64, True),
+    ([0, 0, 64], 1, 1, 64, False),
+]
+
+
+@pytest.mark.parametrize("case", FP8_PACKED, ids=["p%d" % i for i in range(len(FP8_PACKED))])
+def test_fp8_packed_matches_oracle(fa, dev, case):
+    lens, Hq, Hkv, d, causal = case
+    assert sum(lens) % 16 == 0
+    p = make_varlen(lens, Hq, Hkv, d, seed=len(lens) + d + 900, causal=causal)
+    f8 = make_fp8(p)
+    o, lse = _run_packed(fa, f8, dev)
+    q, k, v = f8.dequantized()
+    ref_o, ref_lse = attention_fwd(q, k, v, p.scale, causal, cu_seqlens=p.cu_seqlens)
+    bound, _ = attention_fwd(q, k, np.abs(v), p.scale, causal, cu_seqlens=p.cu_seqlens)
+    _check(o, lse, ref_o, ref_lse, bound, "fp8 packed %s" % (lens,))
+
+
+def test_fp8_d64_from_bf16_with_rotation(fa, dev):
+    """The quantizer and the 8-bit forward at d = 64 together: within the
+    8-bit bound of the oracle on the same dequantized, rotated inputs."""
+    from oracle.fp8 import fp8_dequantize, fp8_quantize
+    from fa_inputs import bf16_bits_to_f32
+    p = make_dense(1, 4, 2, 300, 256, 64, seed=41, causal=True)
+    tb = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+    signs = fa.hadamard_signs(64, 5, dev)
+    q8, qd = fa.fp8_quantize(tb(p.q), signs)
+    k8, kd = fa.fp8_quantize(tb(p.k), signs)
+    vt8, vd = fa.fp8_quantize(tb(p.v), None, transpose=True)
+    o, lse = fa.fwd_fp8(q8, k8, vt8, qd, kd, vd, causal=True, scale=p.scale)
+    torch.cuda.synchronize(dev)
+    s = signs.cpu().numpy()
+    cq, dq = fp8_quantize(bf16_bits_to_f32(p.q), s)
+    ck, dk = fp8_quantize(bf16_bits_to_f32(p.k), s)
+    cv, dv = fp8_quantize(bf16_bits_to_f32(p.v), None)
+    qq, kk, vv = fp8_dequantize(cq, dq), fp8_dequantize(ck, dk), fp8_dequantize(cv, dv)
+    ref_o, ref_lse = attention_fwd(qq, kk, vv, p.scale, True)
+    bound, _ = attention_fwd(qq, kk, np.abs(vv), p.scale, True)
+    _check(o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64), ref_o, ref_lse, bound,
+           "fp8 d64 quantized")
