@@ -20,8 +20,8 @@
 //   code = e4m3(y * inv), round to nearest even, saturating at +-448;
 //   descale = a / (448 sqrt(d)) with rotation, a / 448 without (float64, then
 //         float32), so that code * descale approximates x M (or x).
-// Three launches: slice maxima (accumulated in the descale buffer itself),
-// codes, descales.  No other memory is used.
+// Four launches: zero the slice maxima (accumulated in the descale buffer
+// itself), slice maxima, codes, descales.  No other memory is used.
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -30,6 +30,7 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 namespace fa {
 namespace quant {
@@ -109,8 +110,18 @@ struct Args {
   int tiles;               // blocks per slice
 };
 
+// Zeroes the slice-maximum accumulators (the descale buffer).
+__global__ void zero_kernel(float* descale, int slices) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < slices) descale[i] = 0.f;
+}
+
 template <int D>
 __global__ void __launch_bounds__(THREADS) amax_kernel(const Args a) {
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int slice = blockIdx.x / a.tiles;
   const int r0 = (blockIdx.x % a.tiles) * ROWS_PER_BLOCK + (threadIdx.x / 32) * ROWS_PER_WARP;
   const int lane = threadIdx.x % 32;
@@ -145,6 +156,8 @@ __global__ void __launch_bounds__(THREADS) quant_kernel(const Args a) {
   constexpr int E = D / 32;
   constexpr int PITCH = D + 4;  // bytes per staged row; the 4-byte pad spreads a column over the banks
   __shared__ uint8_t tile[TRANSPOSE ? ROWS_PER_BLOCK * PITCH : 1];
+  grid_dependency_wait();
+  if (threadIdx.x == 0) grid_launch_dependents();
   const int slice = blockIdx.x / a.tiles;
   const int tile_r0 = (blockIdx.x % a.tiles) * ROWS_PER_BLOCK;
   const int r0 = tile_r0 + (threadIdx.x / 32) * ROWS_PER_WARP;
@@ -209,23 +222,38 @@ __global__ void __launch_bounds__(THREADS) quant_kernel(const Args a) {
 }
 
 __global__ void descale_kernel(float* descale, int slices, double divisor) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < slices) descale[i] = static_cast<float>(static_cast<double>(descale[i]) / divisor);
 }
 
+// Four launches, each with programmatic stream serialization (PdlLaunch):
+// zero the accumulators, slice maxima, codes, descales.
 template <int D>
 cudaError_t launch(const Args& a, int slices, bool transpose, cudaStream_t stream) {
   const long long blocks = static_cast<long long>(slices) * a.tiles;
-  if (cudaMemsetAsync(a.descale, 0, sizeof(float) * slices, stream) != cudaSuccess) return cudaGetLastError();
+  const unsigned small = static_cast<unsigned>((slices + 255) / 256);
+  {
+    PdlLaunch L(dim3(small), 256, 0, stream);
+    const cudaError_t e = cudaLaunchKernelEx(&L.cfg, zero_kernel, a.descale, slices);
+    if (e != cudaSuccess) return e;
+  }
   if (blocks == 0) return cudaSuccess;  // no rows: every descale is 0
-  amax_kernel<D><<<static_cast<unsigned>(blocks), THREADS, 0, stream>>>(a);
-  if (transpose)
-    quant_kernel<D, true><<<static_cast<unsigned>(blocks), THREADS, 0, stream>>>(a);
-  else
-    quant_kernel<D, false><<<static_cast<unsigned>(blocks), THREADS, 0, stream>>>(a);
+  {
+    PdlLaunch L(dim3(static_cast<unsigned>(blocks)), THREADS, 0, stream);
+    const cudaError_t e = cudaLaunchKernelEx(&L.cfg, amax_kernel<D>, a);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    PdlLaunch L(dim3(static_cast<unsigned>(blocks)), THREADS, 0, stream);
+    const cudaError_t e = transpose ? cudaLaunchKernelEx(&L.cfg, quant_kernel<D, true>, a)
+                                    : cudaLaunchKernelEx(&L.cfg, quant_kernel<D, false>, a);
+    if (e != cudaSuccess) return e;
+  }
   const double divisor = 448.0 * (a.signs != nullptr ? std::sqrt(static_cast<double>(D)) : 1.0);
-  descale_kernel<<<(slices + 255) / 256, 256, 0, stream>>>(a.descale, slices, divisor);
-  return cudaGetLastError();
+  PdlLaunch L(dim3(small), 256, 0, stream);
+  return cudaLaunchKernelEx(&L.cfg, descale_kernel, a.descale, slices, divisor);
 }
 
 }  // namespace quant

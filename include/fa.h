@@ -188,9 +188,9 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
  * codes do not depend on launch order.
  * Errors: FA_ERR_SHAPE for negative sizes or, with transpose, N not a
  * multiple of 16; FA_ERR_UNSUPPORTED for other d; FA_ERR_NULL / FA_ERR_ALIGN
- * as described; an empty tensor returns FA_OK.  Three kernels are enqueued;
- * descale doubles as the slice-maximum accumulator between them, and no
- * other memory is used.  Argument errors leave the outputs untouched.
+ * as described; an empty tensor returns FA_OK.  Four kernels are enqueued
+ * (zeroing, slice maxima, codes, descales); descale doubles as the
+ * slice-maximum accumulator between them, and no other memory is used.  Argument errors leave the outputs untouched.
  * Non-finite inputs: a NaN element is left out of its slice's maximum and
  * gets a NaN code (0x7F or 0xFF); an infinite element makes its slice's
  * maximum and descale +inf, its own code NaN and every other code of the
