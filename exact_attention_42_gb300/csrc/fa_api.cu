@@ -111,6 +111,9 @@ fa_status fa_device_status(int* bits) {
   const int bv = fa::bwd_status_and_clear();
   if (bv < 0) return FA_ERR_CUDA;
   v |= bv << 9;  // backward kernels: roles 0-2 (dQ) and 4-6 (dK/dV)
+  const int qv = fa::quant_status_and_clear();
+  if (qv < 0) return FA_ERR_CUDA;
+  if (qv) v |= 1 << 16;  // the one-launch quantizer gave up waiting for its copies
   *bits = v;
   return v ? FA_ERR_TIMEOUT : FA_OK;
 }
@@ -179,7 +182,7 @@ fa_status fa_fp8_quantize(const void* x, void* x8, float* descale, int B, int H,
   fa::LaunchEnv env;
   const fa_status st = fa::launch_env(&env);
   if (st != FA_OK) return st;
-  return fa::launch_fp8_quantize(x, x8, descale, B, H, N, d, transpose, signs, stream);
+  return fa::launch_fp8_quantize(x, x8, descale, B, H, N, d, transpose, signs, stream, env);
 }
 
 int fa_bwd_smem_bytes(int d) { return fa::bwd_smem_bytes(d); }

@@ -88,25 +88,6 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
                                ((col & 7) << 1));
 }
 
-__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -151,7 +132,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int tid = threadIdx.x;
   const int warp = tid / 32, lane = tid % 32;
-  const int split = static_cast<int>(cluster_rank());
+  const int split = static_cast<int>(cluster_ctarank());
   const int nsplit = static_cast<int>(gridDim.x);
   const int bh = blockIdx.y;
   const int b = bh / p.Hkv, kvh = bh % p.Hkv;
@@ -402,21 +383,21 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   __syncthreads();
   // ---- merge the CTAs of the cluster through distributed shared memory
-  cluster_sync();
+  cluster_sync_all();
   if (split == 0 && !*abort_flag) {
     const uint32_t base_m = smem_u32(sM), base_l = smem_u32(sL), base_o = smem_u32(sO);
     for (int idx = tid; idx < R * D; idx += THREADS) {
       const int r = idx / D, c = idx % D;
       float m_star = -INFINITY;
-      for (int s = 0; s < nsplit; ++s) m_star = fmaxf(m_star, ld_cluster_f32(cluster_map(base_m + 4 * r, s)));
+      for (int s = 0; s < nsplit; ++s) m_star = fmaxf(m_star, ld_cluster_f32(cluster_addr(base_m + 4 * r, s)));
       float l_star = 0.f, o_star = 0.f;
       if (m_star != -INFINITY) {
         for (int s = 0; s < nsplit; ++s) {
-          const float ms = ld_cluster_f32(cluster_map(base_m + 4 * r, s));
+          const float ms = ld_cluster_f32(cluster_addr(base_m + 4 * r, s));
           if (ms == -INFINITY) continue;
           const float w = ex2_approx(ms - m_star);
-          l_star += w * ld_cluster_f32(cluster_map(base_l + 4 * r, s));
-          o_star += w * ld_cluster_f32(cluster_map(base_o + 4 * idx, s));
+          l_star += w * ld_cluster_f32(cluster_addr(base_l + 4 * r, s));
+          o_star += w * ld_cluster_f32(cluster_addr(base_o + 4 * idx, s));
         }
       }
       const int h = kvh * p.group + r / p.Nq, i = r % p.Nq;
@@ -425,7 +406,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (c == 0) p.lse[row] = l_star > 0.f ? (m_star + __log2f(l_star)) * 0.69314718055994531f : -INFINITY;
     }
   }
-  cluster_sync();  // the other splits keep their shared memory until the merge has read it
+  cluster_sync_all();  // the other splits keep their shared memory until the merge has read it
 }
 
 }  // namespace dec

@@ -71,7 +71,8 @@ fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const 
 int fwd_status_and_clear();  // -1 if the status word cannot be read
 // e4m3 codes and per-(batch, head) descales of a bf16 tensor (fa_quant.cu).
 fa_status launch_fp8_quantize(const void* x, void* x8, float* descale, int B, int H, int N, int d, int transpose,
-                              const int8_t* signs, cudaStream_t stream);
+                              const int8_t* signs, cudaStream_t stream, const LaunchEnv& env);
+int quant_status_and_clear();  // -1 if the status word cannot be read
 fa_status launch_exp2_soft(const float* x, float* y, int n, cudaStream_t stream);
 int fwd_smem_bytes(int d);
 int fwd_threads();

@@ -188,9 +188,14 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
  * codes do not depend on launch order.
  * Errors: FA_ERR_SHAPE for negative sizes or, with transpose, N not a
  * multiple of 16; FA_ERR_UNSUPPORTED for other d; FA_ERR_NULL / FA_ERR_ALIGN
- * as described; an empty tensor returns FA_OK.  Four kernels are enqueued
- * (zeroing, slice maxima, codes, descales); descale doubles as the
- * slice-maximum accumulator between them, and no other memory is used.  Argument errors leave the outputs untouched.
+ * as described; an empty tensor returns FA_OK.  Slices of at most 1024
+ * rows, and unrotated, untransposed slices of at most 4096 rows (d = 128) or
+ * 8192 rows (d = 64), are handled by one kernel launch: a cluster of up to
+ * 16 CTAs per slice holds the slice in shared memory, reads it from global
+ * memory once and combines the CTA maxima through distributed shared memory.
+ * Other slices take four launches (zeroing, slice maxima, codes, descales),
+ * with descale as the slice-maximum accumulator between them.  Both give
+ * identical codes and descales, and no other memory is used.  Argument errors leave the outputs untouched.
  * Non-finite inputs: a NaN element is left out of its slice's maximum and
  * gets a NaN code (0x7F or 0xFF); an infinite element makes its slice's
  * maximum and descale +inf, its own code NaN and every other code of the
@@ -210,7 +215,8 @@ const char* fa_status_string(fa_status s);
  * a bit and the kernel leaves cleanly.  Bits 0-4: roles of the fa_fwd kernel
  * (K/V producer, MMA issuer, softmax of query tiles 0 and 1, Q loader);
  * bit 8: the split-KV kernel; bits 9-11 and 13-15: producer, MMA issuer and
- * softmax roles of fa_bwd's dQ and dK/dV kernels.  Returns FA_OK and stores
+ * softmax roles of fa_bwd's dQ and dK/dV kernels; bit 16: fa_fp8_quantize's
+ * one-launch kernel.  Returns FA_OK and stores
  * 0 in *bits when nothing went wrong, FA_ERR_TIMEOUT with the bits otherwise.
  * The call first waits for all work on the current device (every stream,
  * cudaDeviceSynchronize), so no kernel can set a bit between the read and the

@@ -60,6 +60,16 @@ CASES = [
     (2, 2, 208, 128, True, True, False),     # transposed, 208 = 3 blocks + 16 rows
     (1, 3, 64, 64, False, True, True),
     (1, 1, 1000, 128, True, False, True),    # many blocks per slice
+    # The one-launch path takes slices of up to 1024 rows (above) and plain
+    # slices up to its shared-memory limit (a 16-CTA cluster per slice) ...
+    (2, 2, 4096, 128, False, False, True),
+    (1, 1, 8192, 64, False, False, False),
+    # ... the four-launch path large rotated or transposed slices, and slices
+    # past that limit.
+    (1, 2, 4096, 128, False, True, False),
+    (1, 1, 8192, 64, True, False, True),
+    (1, 2, 4160, 128, False, False, False),
+    (1, 1, 8208, 64, False, True, False),
 ]
 
 
