@@ -19,7 +19,8 @@ constexpr int kFaultFwd = 1;     // fa_fwd_kernel's K/V producer
 constexpr int kFaultDecode = 2;  // decode_kernel's K/V producer
 constexpr int kFaultBwdDq = 3;   // bwd_dq_kernel's K/V producer
 constexpr int kFaultBwdDkdv = 4; // bwd_dkdv_kernel's Q/dO producer
-constexpr int kFaultModes = 5;
+constexpr int kFaultQuant = 5;   // quant_fused_kernel's first bulk copy in every CTA
+constexpr int kFaultModes = 6;
 
 // Launch configuration with programmatic stream serialization: the kernel
 // may start before the previous kernel in `stream` has finished, runs its

@@ -111,6 +111,7 @@ struct Args {
   const int8_t* signs;     // [D] or nullptr
   int N;
   int tiles;               // blocks per slice
+  int fault_inject;        // test hook (one-launch path): 1 = the first bulk copy of every CTA is withheld
 };
 
 // Zeroes the slice-maximum accumulators (the descale buffer).
@@ -330,6 +331,7 @@ __global__ void __launch_bounds__(FTHREADS) quant_fused_kernel(const Args a, int
   const __nv_bfloat16* src = a.x + (static_cast<long long>(slice) * a.N + r0) * D;
   if (tid == 0) {
     for (int c = 0; c < nchunks; ++c) {
+      if (a.fault_inject && c == 0) continue;  // test hook: this copy never arrives
       const uint32_t bytes = static_cast<uint32_t>(min(FCHUNK, nrows - c * FCHUNK) * D * 2);
       mbar_arrive_expect_tx(smem_u32(&bars[c]), bytes);
       bulk_load(smem_u32(xs + c * FCHUNK * D), src + static_cast<long long>(c) * FCHUNK * D, bytes,
@@ -534,6 +536,7 @@ fa_status launch_fp8_quantize(const void* x, void* x8, float* descale, int B, in
   a.signs = signs;
   a.N = N;
   a.tiles = (N + quant::ROWS_PER_BLOCK - 1) / quant::ROWS_PER_BLOCK;
+  a.fault_inject = env.fault_mode == kFaultQuant ? 1 : 0;
   const int slices = B * H;
   const cudaError_t e = d == 128 ? quant::launch<128>(a, slices, transpose != 0, stream, env.sms, env.wait_limit_ns)
                                  : quant::launch<64>(a, slices, transpose != 0, stream, env.sms, env.wait_limit_ns);

@@ -232,7 +232,8 @@ fa_status fa_device_status(int* bits);
  *   1  fa_fwd's kernel (its K/V producer; status bits 0-4),
  *   2  the split-KV kernel of fa_decode and fa_fwd (status bit 8),
  *   3  fa_bwd's dQ kernel (its K/V producer; bits 9-11),
- *   4  fa_bwd's dK/dV kernel (its Q/dO producer; bits 13-15).
+ *   4  fa_bwd's dK/dV kernel (its Q/dO producer; bits 13-15),
+ *   5  fa_fp8_quantize's one-launch kernel (its first bulk copy; bit 16).
  * The kernel then records the bits in its device status word, waits (bounded)
  * for its own copies in flight, frees its Tensor Memory and exits, leaving the
  * CUDA context usable; its outputs are undefined.  wait_limit_seconds

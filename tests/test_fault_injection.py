@@ -4,9 +4,9 @@ status bits, exit cleanly and leave the context usable.
 
 Modes of fa_debug_fault_injection (include/fa.h): 1 the forward kernel's K/V
 producer, 2 the split-KV kernel's producer, 3 the backward dQ kernel's K/V
-producer, 4 the backward dK/dV kernel's Q/dO producer withhold their first
-copy.  Each case then runs the same problem again and checks it against the
-oracle."""
+producer, 4 the backward dK/dV kernel's Q/dO producer, 5 the one-launch
+quantizer withhold their first copy.  Each case then runs the same problem
+again and checks it against the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -19,7 +19,7 @@ def test_hook_argument_checks():
     import exact_attention_42_gb300 as fa
     fa.build()
     with pytest.raises(fa.FaError):
-        fa.fa_debug_fault_injection(5, 0.1)
+        fa.fa_debug_fault_injection(6, 0.1)
     with pytest.raises(fa.FaError):
         fa.fa_debug_fault_injection(-1, 0.1)
     with pytest.raises(fa.FaError):
@@ -112,3 +112,26 @@ def test_bwd_withheld_fill_times_out_and_context_survives(mode, mask, name):
         big = float(np.max(np.abs(want)))
         err = float(np.max(np.abs(got - want)))
         assert err <= 2e-2 * big, "%s after fault injection: max err %.3g of max |ref| %.3g" % (nm, err, big)
+
+
+@pytest.mark.gpu
+def test_quantizer_withheld_copy_times_out_and_context_survives():
+    import exact_attention_42_gb300 as fa
+    from fa_inputs import bf16_bits_to_f32, normal_bf16, stream_key
+    from oracle.fp8 import fp8_quantize
+    fa.build()
+    dev = torch.device("cuda", 0)
+    bits = normal_bf16(stream_key(77, 1), (2, 3, 700, 128))   # 700 rows: the one-launch path
+    x = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def run():
+        r = fa.fp8_quantize(x, None)
+        torch.cuda.synchronize(dev)
+        return r
+    assert _inject(fa, 1, run) == 0          # other kernels' modes leave the quantizer alone
+    bits_set = _inject(fa, 5, run)
+    assert bits_set == 1 << 16, "the quantizer should report bit 16 (bits=%#x)" % bits_set
+    x8, desc = run()
+    assert fa.fa_device_status() == 0
+    ref8, ref_desc = fp8_quantize(bf16_bits_to_f32(bits), None)
+    assert np.array_equal(x8.cpu().numpy(), ref8) and np.array_equal(desc.cpu().numpy(), ref_desc)
