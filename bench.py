@@ -47,9 +47,11 @@ FP8_OVER_BF16 = 2.0   # nominal dense fp8 : bf16 tensor rate (4.5 : 2.25 PFLOP/s
 UNIT = "TFLOP/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = {
-    "fa_fwd_kernel": ["exact_attention_42_gb300/csrc/fa_fwd.cu", "exact_attention_42_gb300/csrc/ptx.cuh"],
+    "fa_fwd_kernel": ["exact_attention_42_gb300/csrc/fa_fwd.cu", "exact_attention_42_gb300/csrc/ptx.cuh",
+                      "exact_attention_42_gb300/csrc/fa_sched.cu"],
     "decode_kernel": ["exact_attention_42_gb300/csrc/fa_decode.cu", "exact_attention_42_gb300/csrc/ptx.cuh"],
-    "fa_bwd": ["exact_attention_42_gb300/csrc/fa_bwd.cu", "exact_attention_42_gb300/csrc/ptx.cuh"],
+    "fa_bwd": ["exact_attention_42_gb300/csrc/fa_bwd.cu", "exact_attention_42_gb300/csrc/ptx.cuh",
+               "exact_attention_42_gb300/csrc/fa_sched.cu"],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 ROTATE = 3            # input copies cycled through, so each step reads from HBM

@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd_smem_bytes.restype = ci
             L.fa_fp8_quantize.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp, vp]
             L.fa_fp8_quantize.restype = ci
+            L.fa_debug_schedule.argtypes = [ci] * 9 + [vp, vp, ci, ctypes.POINTER(ci)]
+            L.fa_debug_schedule.restype = ci
             _lib = L
     return _lib
 
@@ -135,6 +137,24 @@ def fa_debug_fwd_pair(on: int) -> None:
     st = lib().fa_debug_fwd_pair(int(on))
     if st != 0:
         raise FaError(st, "fa_debug_fwd_pair")
+
+
+def fa_debug_schedule(kernel: int, B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, causal: bool,
+                      workers: int):
+    """The worker lists a persistent launch would run (see fa.h): a list of unit
+    lists, one per worker, or None when the kernel uses its built-in order."""
+    cap = 1 << 16
+    start = (ctypes.c_int32 * (workers + 1))()
+    units = (ctypes.c_int32 * cap)()
+    n = ctypes.c_int(0)
+    st = lib().fa_debug_schedule(int(kernel), B, Hq, Hkv, Nq, Nk, d, int(bool(causal)), workers,
+                                 ctypes.cast(start, ctypes.c_void_p), ctypes.cast(units, ctypes.c_void_p), cap,
+                                 ctypes.byref(n))
+    if st != 0:
+        raise FaError(st, "fa_debug_schedule")
+    if n.value == 0:
+        return None
+    return [list(units[start[w]:start[w + 1]]) for w in range(n.value)]
 
 
 def fa_debug_exp2_soft(x_ptr: int, y_ptr: int, n: int, stream: int = 0) -> None:

@@ -10,7 +10,8 @@ ROOT = os.path.dirname(PKG_DIR)
 CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG_DIR, "libfa.so")
-SOURCES = [os.path.join(CSRC, n) for n in ("fa_api.cu", "fa_fwd.cu", "fa_decode.cu", "fa_bwd.cu", "fa_quant.cu")]
+SOURCES = [os.path.join(CSRC, n)
+           for n in ("fa_api.cu", "fa_fwd.cu", "fa_decode.cu", "fa_bwd.cu", "fa_quant.cu", "fa_sched.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "fa_internal.h"), os.path.join(INCLUDE, "fa.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <memory>
 #include <mutex>
 
 #include "fa.h"
@@ -233,6 +234,29 @@ fa_status fa_debug_soft_exp(int on) {
 fa_status fa_debug_fwd_pair(int on) {
   if (on != 0 && on != 1) return FA_ERR_VALUE;
   fa::g_fwd_pair.store(on);
+  return FA_OK;
+}
+
+fa_status fa_debug_schedule(int kernel, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int workers,
+                             int32_t* start, int32_t* units, int capacity, int* table_workers) {
+  if (start == nullptr || units == nullptr || table_workers == nullptr) return FA_ERR_NULL;
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nq < 0 || Nk < 0 || workers < 1) return FA_ERR_SHAPE;
+  if (d != 64 && d != 128) return FA_ERR_SHAPE;
+  std::unique_ptr<fa::SchedTable> sc(new fa::SchedTable);
+  bool ok = false;
+  if (kernel == 0 || kernel == 1)
+    ok = fa::fwd_schedule_for(kernel, B, Hq, Hkv, Nq, Nk, d, causal, workers, sc.get());
+  else if (kernel == 2 || kernel == 3)
+    ok = fa::bwd_schedule_for(kernel - 2, B, Hq, Hkv, Nq, Nk, d, causal, workers, sc.get());
+  else
+    return FA_ERR_VALUE;
+  if (!ok) return FA_ERR_SHAPE;
+  *table_workers = sc->workers;
+  if (sc->workers == 0) return FA_OK;
+  const int n = sc->start[sc->workers];
+  if (capacity < n) return FA_ERR_SHAPE;
+  for (int w = 0; w <= sc->workers; ++w) start[w] = sc->start[w];
+  for (int i = 0; i < n; ++i) units[i] = sc->unit[i];
   return FA_OK;
 }
 

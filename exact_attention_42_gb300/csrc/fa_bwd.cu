@@ -39,9 +39,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <cstring>
-#include <cmath>
 #include <mutex>
 
 #include "fa.h"
@@ -263,11 +264,11 @@ struct QUnit {
 };
 
 // Dense: unit u -> (batch*head, query tile), later query tiles (more visible
-// keys under a causal mask) first, so the static schedule deals the heaviest
-// units first.  (Dealing them by groups of heads instead, so that concurrent
-// CTAs share K/V in L2, cut DRAM reads threefold on GB300 but not the time,
-// and slowed the dK/dV kernel by unbalancing the schedule.)  Packed: u =
-// blk * Hq + h over every sequence's tiles, a sequence's last tile first.
+// keys under a causal mask) first, so the snake order deals the heaviest
+// units first.  Dense launches normally run host-built worker lists instead
+// (SchedTable: head groups in turn, list-scheduled by cost); a static deal by
+// head groups would unbalance the CTAs.  Packed: u = blk * Hq + h over every
+// sequence's tiles, a sequence's last tile first.
 __device__ __forceinline__ bool dq_unit(const Params& p, int u, QUnit& w) {
   if (p.cu_seqlens == nullptr) {
     const int bh_count = p.B * p.Hq;
@@ -307,7 +308,7 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const Params p) {
+                  const Params p, const __grid_constant__ SchedTable sc) {
   using C = Cfg<D, false>;
   constexpr bool KV_KERNEL = false;
   extern __shared__ uint8_t smem_raw[];
@@ -333,7 +334,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t s_free_bar = bar_base + 8u * (2 * C::NS + 3);
   const uint32_t dp_full_bar = bar_base + 8u * (2 * C::NS + 10);
   const uint32_t dp_free_bar = bar_base + 8u * (2 * C::NS + 11);
-  const uint32_t ds_full_bar = bar_base + 8u * (2 * C::NS + 4);
+  // One dS-full barrier per dS buffer: the issuer waits for dS(g) only after
+  // issuing S(g+1) and dP(g+1), so with a single barrier the softmax could
+  // complete two phases before the issuer looks and a parity wait would miss
+  // them.  dS(g+2) goes into buffer g & 1 only after dQ(g) has read it, so a
+  // buffer's barrier can never run a phase ahead.
+  auto ds_full_bar = [&](uint32_t b) { return bar_base + 8u * (2 * C::NS + (b ? 12 : 4)); };
   auto ds_free_bar = [&](int b) { return bar_base + 8u * (2 * C::NS + 5 + b); };
   const uint32_t dq_done_bar = bar_base + 8u * (2 * C::NS + 7);
   const uint32_t dq_free_bar = bar_base + 8u * (2 * C::NS + 8);
@@ -353,7 +359,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(s_free_bar, SOFTMAX_WARPS);
     mbar_init(dp_full_bar, 1);
     mbar_init(dp_free_bar, SOFTMAX_WARPS);
-    mbar_init(ds_full_bar, SOFTMAX_WARPS);
+    mbar_init(ds_full_bar(0), SOFTMAX_WARPS);
+    mbar_init(ds_full_bar(1), SOFTMAX_WARPS);
     mbar_init(ds_free_bar(0), 1);
     mbar_init(ds_free_bar(1), 1);
     mbar_init(dq_done_bar, 1);
@@ -375,7 +382,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   grid_dependency_wait();
   if (threadIdx.x == 0) grid_launch_dependents();
   const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_tiles(p) * (KV_KERNEL ? p.Hkv : p.Hq);
-  const int nrounds = (num_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  // Dense problems run the host-built worker lists (SchedTable), packed ones the snake order.
+  const bool table = sc.workers == static_cast<int>(gridDim.x) && p.cu_seqlens == nullptr;
+  const int slot0 = table ? sc.start[blockIdx.x] : 0;
+  const int nrounds = table ? sc.start[blockIdx.x + 1] - slot0
+                            : (num_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  auto unit_at = [&](int k) { return table ? static_cast<int>(sc.unit[slot0 + k]) : snake_unit(k); };
 
   if (warp == WARP_PRODUCER) {
     if (lane == 0) {
@@ -388,7 +400,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t it = 0, qfills = 0;
       bool ok = true;
       for (int k = 0; k < nrounds && ok; ++k) {
-        const int u = snake_unit(k);
+        const int u = unit_at(k);
         if (u >= num_units) continue;
         QUnit w;
         if (!dq_unit(p, u, w)) continue;
@@ -442,7 +454,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t it = 0, gt = 0, units_done = 0, qcnt = 0;
     bool ok = true;
     for (int k = 0; k < nrounds && ok; ++k) {
-      const int u = snake_unit(k);
+      const int u = unit_at(k);
       if (u >= num_units) continue;
       QUnit w;
       if (!dq_unit(p, u, w)) continue;
@@ -490,7 +502,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int j = 0; j < nkv && ok; ++j) {
         const uint32_t g = gt + j;
         if (j + 1 < nkv && !(ok = issue_s(j + 1) && issue_dp(j + 1))) break;
-        if (!(ok = wait_or_abort(ds_full_bar, g & 1u, abort_flag, 1, p.wait_limit_ns))) break;
+        if (!(ok = wait_or_abort(ds_full_bar(g & 1u), (g >> 1) & 1u, abort_flag, 1, p.wait_limit_ns))) break;
         if (j == 0 && units_done > 0 &&
             !(ok = wait_or_abort(dq_free_bar, (units_done - 1) & 1u, abort_flag, 1, p.wait_limit_ns)))
           break;
@@ -527,7 +539,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t gt = 0, units_done = 0;
     bool ok = true;
     for (int k = 0; k < nrounds && ok; ++k) {
-      const int u = snake_unit(k);
+      const int u = unit_at(k);
       if (u >= num_units) continue;
       QUnit w;
       if (!dq_unit(p, u, w)) continue;
@@ -603,7 +615,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         warp_arrive(dp_free_bar);
         tmem_wait_st();
         tc_fence_before();
-        warp_arrive(ds_full_bar);
+        warp_arrive(ds_full_bar(g & 1u));
       }
       if (!ok) break;
       // ------------------------------------------------------------ epilogue
@@ -698,7 +710,7 @@ template <int D>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                    const Params p) {
+                    const Params p, const __grid_constant__ SchedTable sc) {
   using C = Cfg<D, true>;
   constexpr bool KV_KERNEL = true;
   extern __shared__ uint8_t smem_raw[];
@@ -771,7 +783,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   grid_dependency_wait();
   if (threadIdx.x == 0) grid_launch_dependents();
   const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_tiles(p) * (KV_KERNEL ? p.Hkv : p.Hq);
-  const int nrounds = (num_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  // Dense problems run the host-built worker lists (SchedTable), packed ones the snake order.
+  const bool table = sc.workers == static_cast<int>(gridDim.x) && p.cu_seqlens == nullptr;
+  const int slot0 = table ? sc.start[blockIdx.x] : 0;
+  const int nrounds = table ? sc.start[blockIdx.x + 1] - slot0
+                            : (num_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  auto unit_at = [&](int k) { return table ? static_cast<int>(sc.unit[slot0 + k]) : snake_unit(k); };
 
   if (warp == WARP_PRODUCER) {
     if (lane == 0) {
@@ -782,7 +799,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t it = 0, kvfills = 0;
       bool ok = true;
       for (int k = 0; k < nrounds && ok; ++k) {
-        const int u = snake_unit(k);
+        const int u = unit_at(k);
         if (u >= num_units) continue;
         KUnit w;
         if (!kv_unit(p, u, w)) continue;
@@ -838,7 +855,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t it = 0, gt = 0, units_done = 0, kvcnt = 0;
     bool ok = true;
     for (int k = 0; k < nrounds && ok; ++k) {
-      const int u = snake_unit(k);
+      const int u = unit_at(k);
       if (u >= num_units) continue;
       KUnit w;
       if (!kv_unit(p, u, w)) continue;
@@ -934,7 +951,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t gt = 0, units_done = 0;
     bool ok = true;
     for (int k = 0; k < nrounds && ok; ++k) {
-      const int u = snake_unit(k);
+      const int u = unit_at(k);
       if (u >= num_units) continue;
       KUnit w;
       if (!kv_unit(p, u, w)) continue;
@@ -1116,6 +1133,65 @@ int bwd_smem_bytes(int d) {  // the larger of the two main kernels
   return 0;
 }
 
+// The schedule builder's view of a dense backward unit, in dq_unit's and
+// kv_unit's order.  dQ kernel: cost = K/V tiles visited; dK/dV kernel: cost =
+// query tiles visited over the group's query heads; plus one step of per-unit
+// overhead.  Group: the unit's KV head's group.
+struct BwdSchedCtx {
+  int B, Hq, Hkv, Nq, Nk, causal, nqt, nkt, group_heads;
+  bool kv;
+};
+
+static void describe_bwd_unit(const void* vctx, int u, SchedUnit* out) {
+  const BwdSchedCtx& c = *static_cast<const BwdSchedCtx*>(vctx);
+  const int group = c.Hq / c.Hkv;
+  int steps = 0, kv_head = 0;
+  if (!c.kv) {
+    const int bh_count = c.B * c.Hq;
+    const int q0 = (c.nqt - 1 - u / bh_count) * bwd::TILE, bh = u % bh_count;
+    kv_head = (bh / c.Hq) * c.Hkv + (bh % c.Hq) / group;
+    int last_key = c.Nk - 1;
+    if (c.causal) last_key = std::min(last_key, std::min(q0 + bwd::TILE - 1, c.Nq - 1) + (c.Nk - c.Nq));
+    steps = (q0 < c.Nq && last_key >= 0) ? last_key / bwd::TILE + 1 : 0;
+  } else {
+    const int n = c.B * c.Hkv;
+    const int key0 = (u / n) * bwd::TILE;
+    kv_head = u % n;
+    int first = 0;
+    if (c.causal) {
+      const int q_min = key0 - (c.Nk - c.Nq);
+      first = q_min <= 0 ? 0 : (q_min >= c.Nq ? c.nqt : q_min / bwd::TILE);
+    }
+    steps = group * (c.nqt - first);
+  }
+  out->cost = static_cast<float>(steps) + 1.0f;
+  out->group = kv_head / c.group_heads;
+}
+
+static void bwd_schedule(SchedTable* sc, bool kv, int B, int Hq, int Hkv, int Nq, int Nk, int D, int causal, int nqt,
+                         int nkt, long long units, long long grid) {
+  sc->workers = 0;
+  if (units > kSchedCap || grid > kSchedMaxWorkers || units <= grid) return;
+  // Bytes one KV head's units stream: K and V (dQ kernel), or Q and dO of the
+  // head's query group (dK/dV kernel).
+  const double bytes =
+      kv ? 2.0 * (Hq / Hkv) * static_cast<double>(Nq) * D * 2 : 2.0 * static_cast<double>(Nk) * D * 2;
+  BwdSchedCtx c{B, Hq, Hkv, Nq, Nk, causal, nqt, nkt, sched_group_heads(bytes), kv};
+  const long long key[12] = {kv ? 3 : 2, B, Hq, Hkv, Nq, Nk, D, causal, grid, 0, 0, 0};
+  build_schedule(key, static_cast<int>(grid), static_cast<int>(units), describe_bwd_unit, &c, sc);
+}
+
+bool bwd_schedule_for(int kv, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int workers,
+                      SchedTable* sc) {
+  const int nqt = (Nq + bwd::TILE - 1) / bwd::TILE, nkt = (Nk + bwd::TILE - 1) / bwd::TILE;
+  const long long units = static_cast<long long>(B) * (kv ? static_cast<long long>(Hkv) * nkt
+                                                          : static_cast<long long>(Hq) * nqt);
+  const long long grid = units < workers ? units : workers;
+  sc->workers = 0;
+  if (grid > 0) bwd_schedule(sc, kv != 0, B, Hq, Hkv, Nq, Nk, d, causal ? 1 : 0, nqt, nkt, units, grid);
+  return true;
+}
+
 template <int D>
 static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const void* o, const void* dout,
                               const float* lse, void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv,
@@ -1196,7 +1272,11 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
     const long long grid = units < sms ? units : sms;
     if (grid > 0) {
       PdlLaunch L(dim3(static_cast<unsigned>(grid)), bwd::NUM_THREADS, CQ::SMEM_BYTES, stream);
-      if (cudaLaunchKernelEx(&L.cfg, bwd::bwd_dq_kernel<D>, tq, tdo, tk, tv, prm) != cudaSuccess) return FA_ERR_CUDA;
+      SchedTable sc;
+      sc.workers = 0;
+      if (!packed) bwd_schedule(&sc, false, B, Hq, Hkv, Nq, Nk, D, prm.causal, prm.nqt, prm.nkt, units, grid);
+      if (cudaLaunchKernelEx(&L.cfg, bwd::bwd_dq_kernel<D>, tq, tdo, tk, tv, prm, sc) != cudaSuccess)
+        return FA_ERR_CUDA;
     }
   }
   // dK, dV: one unit per (batch or sequence, key/value head, key tile).
@@ -1208,7 +1288,11 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
     const long long grid = units < sms ? units : sms;
     if (grid > 0) {
       PdlLaunch L(dim3(static_cast<unsigned>(grid)), bwd::NUM_THREADS, CKV::SMEM_BYTES, stream);
-      if (cudaLaunchKernelEx(&L.cfg, bwd::bwd_dkdv_kernel<D>, tq, tdo, tk, tv, prm) != cudaSuccess) return FA_ERR_CUDA;
+      SchedTable sc;
+      sc.workers = 0;
+      if (!packed) bwd_schedule(&sc, true, B, Hq, Hkv, Nq, Nk, D, prm.causal, prm.nqt, prm.nkt, units, grid);
+      if (cudaLaunchKernelEx(&L.cfg, bwd::bwd_dkdv_kernel<D>, tq, tdo, tk, tv, prm, sc) != cudaSuccess)
+        return FA_ERR_CUDA;
     }
   }
   return FA_OK;

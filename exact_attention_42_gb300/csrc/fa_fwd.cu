@@ -40,6 +40,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <cmath>
@@ -341,7 +342,8 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, const 
 template <int D, bool FP8, int SOFT, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                  const __grid_constant__ CUtensorMap tm_v, const Params p,
+                  const __grid_constant__ SchedTable sc) {
   using C = Cfg<D, FP8, PAIR>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
@@ -418,9 +420,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // is spread evenly (with the 1:16 cost range of a causal head the busiest
   // worker stays within a few percent of the mean, against 13% for plain
   // round-robin).
+  // With a host-built table (dense problems) worker w runs its own list of
+  // units instead (SchedTable: head groups visited in turn, longest first).
   const int G = static_cast<int>(gridDim.x) / C::CTAS;
   const int worker = static_cast<int>(blockIdx.x) / C::CTAS;
-  auto snake_unit = [&](int k) { return k * G + ((k & 1) ? (G - 1 - worker) : worker); };
+  const bool table = sc.workers == G && p.cu_seqlens == nullptr;
+  const int slot0 = table ? sc.start[worker] : 0;
+  const int slots = table ? sc.start[worker + 1] - slot0 : (num_units + G - 1) / G;
+  auto snake_unit = [&](int k) {
+    return table ? static_cast<int>(sc.unit[slot0 + k]) : k * G + ((k & 1) ? (G - 1 - worker) : worker);
+  };
   auto tiles_of = [&](const Unit& w, int t) { return kv_tiles(p, w, t, C::TILE_ROWS); };
 
   if (warp >= 8) {
@@ -439,8 +448,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // (another head); warming them into L2 a few K/V tiles before the
       // current unit ends hides most of that latency at the unit boundary.
       auto prefetch_next_unit = [&](int k_next) {
+        if (k_next >= slots) return;
         const int un = snake_unit(k_next);
-        if (k_next * G >= num_units || un >= num_units) return;
+        if (un >= num_units) return;
         Unit wn;
         if (!decode_unit(p, un, wn, C::UNIT_ROWS)) return;
         const int nk0 = tiles_of(wn, 0), nk1 = tiles_of(wn, 1);
@@ -465,7 +475,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
       };
-      for (int k = 0; k * G < num_units && ok; ++k) {
+      for (int k = 0; k < slots && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= num_units) continue;
         Unit w;
@@ -525,7 +535,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t qfills[NQT] = {0, 0};
       bool ok = true;
-      for (int k = 0; k * G < num_units && ok; ++k) {
+      for (int k = 0; k < slots && ok; ++k) {
         const int u = snake_unit(k);
         if (u >= num_units) continue;
         Unit w;
@@ -638,7 +648,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t it = 0;
     uint32_t qcnt[NQT] = {0, 0}, pcnt[NQT] = {0, 0};
     bool ok = true;
-    for (int k = 0; k * G < num_units && ok; ++k) {
+    for (int k = 0; k < slots && ok; ++k) {
       const int u = snake_unit(k);
       if (u >= num_units) continue;
       Unit w;
@@ -751,7 +761,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     uint32_t scnt = 0, ocnt = 0;
     bool ok = true;
-    for (int k = 0; k * G < num_units && ok; ++k) {
+    for (int k = 0; k < slots && ok; ++k) {
       const int u = snake_unit(k);
       if (u >= num_units) continue;
       Unit w;
@@ -1047,9 +1057,46 @@ static bool prepare_kernel(int device, int* pairs = nullptr) {
 // see PdlLaunch) as `clusters` clusters of `cta_per` CTAs.
 template <typename Kernel>
 static fa_status launch_kernel(Kernel kernel, long long clusters, int cta_per, int smem, cudaStream_t stream,
-                               const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const Params& prm) {
+                               const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const Params& prm,
+                               const SchedTable& sc) {
   PdlLaunch L(dim3(static_cast<unsigned>(clusters * cta_per)), NUM_THREADS, smem, stream, static_cast<unsigned>(cta_per));
-  return cudaLaunchKernelEx(&L.cfg, kernel, tq, tk, tv, prm) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  return cudaLaunchKernelEx(&L.cfg, kernel, tq, tk, tv, prm, sc) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// The schedule builder's view of a dense forward unit (decode_unit's order):
+// cost = K/V steps of its longer query tile plus one step of per-unit
+// overhead; group = its KV head's group.
+struct FwdSchedCtx {
+  int B, Hq, Hkv, Nq, Nk, causal, unit_rows, tile_rows, nqb, group_heads;
+};
+
+static void describe_fwd_unit(const void* vctx, int u, SchedUnit* out) {
+  const FwdSchedCtx& c = *static_cast<const FwdSchedCtx*>(vctx);
+  const int bh_count = c.B * c.Hq;
+  const int qb = c.nqb - 1 - u / bh_count;
+  const int bh = u % bh_count;
+  const int kv_head = (bh / c.Hq) * c.Hkv + (bh % c.Hq) / (c.Hq / c.Hkv);
+  int steps = 0;
+  for (int t = 0; t * c.tile_rows < c.unit_rows; ++t) {
+    const int q0 = qb * c.unit_rows + t * c.tile_rows;
+    if (q0 >= c.Nq || c.Nk <= 0) continue;
+    int last_key = c.Nk - 1;
+    if (c.causal) last_key = std::min(last_key, std::min(q0 + c.tile_rows - 1, c.Nq - 1) + (c.Nk - c.Nq));
+    if (last_key >= 0) steps = std::max(steps, last_key / BLOCK_N + 1);
+  }
+  out->cost = static_cast<float>(steps) + 1.0f;
+  out->group = kv_head / c.group_heads;
+}
+
+// Table for a dense single-CTA launch of `grid` workers (workers = 0: snake).
+static void fwd_schedule(SchedTable* sc, int kind, int B, int Hq, int Hkv, int Nq, int Nk, int D, int elem_bytes,
+                         int causal, int unit_rows, int nqb, long long units, long long grid) {
+  sc->workers = 0;
+  if (units > kSchedCap || grid > kSchedMaxWorkers || units <= grid) return;
+  FwdSchedCtx c{B, Hq, Hkv, Nq, Nk, causal, unit_rows, BLOCK_M, nqb,
+                sched_group_heads(2.0 * static_cast<double>(Nk) * D * elem_bytes)};
+  const long long key[12] = {kind, B, Hq, Hkv, Nq, Nk, D, causal, unit_rows, grid, elem_bytes, 0};
+  build_schedule(key, static_cast<int>(grid), static_cast<int>(units), describe_fwd_unit, &c, sc);
 }
 
 template <int D>
@@ -1120,15 +1167,19 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
     grid = units < workers ? units : workers;
   }
   if (grid <= 0) return FA_OK;
+  SchedTable sc;
+  sc.workers = 0;
+  if (!packed && !pair)
+    fwd_schedule(&sc, 0, B, Hq, Hkv, Nq, Nk, D, 2, prm.causal, unit_rows, prm.nqb, prm.num_units, grid);
   if constexpr (D == 128) {
     if (pair)
       return launch_kernel(fa_fwd_kernel<D, false, 0, true>, grid, 2, Cfg<D, false, true>::SMEM_BYTES, stream, tq,
-                           tk, tv, prm);
+                           tk, tv, prm, sc);
   }
   if (soft)
     return launch_kernel(fa_fwd_kernel<D, false, SOFT_EXP_PERIOD, false>, grid, 1, Cfg<D>::SMEM_BYTES, stream, tq, tk,
-                         tv, prm);
-  return launch_kernel(fa_fwd_kernel<D, false, 0, false>, grid, 1, Cfg<D>::SMEM_BYTES, stream, tq, tk, tv, prm);
+                         tv, prm, sc);
+  return launch_kernel(fa_fwd_kernel<D, false, 0, false>, grid, 1, Cfg<D>::SMEM_BYTES, stream, tq, tk, tv, prm, sc);
 }
 
 fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
@@ -1207,10 +1258,15 @@ static fa_status launch_fp8(const void* q8, const void* k8, const void* vt8, con
     grid = units < env.sms ? units : env.sms;
   }
   if (grid <= 0) return FA_OK;
+  // The 8-bit path keeps the snake order: its K/V tiles are half the bytes,
+  // its DRAM traffic is already close to the algorithmic bytes, and the
+  // worker lists measured 0.4% slower on the headline workload.
+  SchedTable sc;
+  sc.workers = 0;
   if (soft)
     return launch_kernel(fa_fwd_kernel<D, true, SOFT_EXP_PERIOD, false>, grid, 1, C::SMEM_BYTES, stream, tq, tk, tv,
-                         prm);
-  return launch_kernel(fa_fwd_kernel<D, true, 0, false>, grid, 1, C::SMEM_BYTES, stream, tq, tk, tv, prm);
+                         prm, sc);
+  return launch_kernel(fa_fwd_kernel<D, true, 0, false>, grid, 1, C::SMEM_BYTES, stream, tq, tk, tv, prm, sc);
 }
 
 fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const float* q_descale,
@@ -1222,6 +1278,20 @@ fa_status launch_fwd_fp8(const void* q8, const void* k8, const void* vt8, const 
                           cu_seqlens, stream, env);
   return launch_fp8<128>(q8, k8, vt8, q_descale, k_descale, v_descale, o, lse, B, Hq, Hkv, Nq, Nk, scale, causal,
                          cu_seqlens, stream, env);
+}
+
+bool fwd_schedule_for(int fp8, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int workers,
+                      SchedTable* sc) {
+  sc->workers = 0;
+  if (fp8) return true;  // the 8-bit launch runs the snake order
+  const int unit_rows = NQT * BLOCK_M;
+  const int nqb = (Nq + unit_rows - 1) / unit_rows;
+  const long long units = static_cast<long long>(B) * Hq * nqb;
+  const long long grid = units < workers ? units : workers;
+  sc->workers = 0;
+  if (grid <= 0) return true;
+  fwd_schedule(sc, 0, B, Hq, Hkv, Nq, Nk, d, 2, causal ? 1 : 0, unit_rows, nqb, units, grid);
+  return true;
 }
 
 int fwd_status_and_clear() {

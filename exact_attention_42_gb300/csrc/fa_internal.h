@@ -59,6 +59,48 @@ struct LaunchEnv {
   int fwd_pair = 0;                     // test hook, see fa_debug_fwd_pair
 };
 
+// Unit lists of a persistent launch, one per worker (CTA, or CTA pair),
+// handed to the kernel by value as a __grid_constant__ parameter, so they need
+// no device memory.  Worker w runs units unit[start[w] .. start[w+1]) in that
+// order.  workers == 0 means no table: the kernel deals units in its static
+// snake order instead (packed sequences, whose lengths the host does not
+// know, and problems larger than the table).
+constexpr int kSchedMaxWorkers = 160;
+constexpr int kSchedCap = 4096;
+struct SchedTable {
+  int workers;
+  uint16_t start[kSchedMaxWorkers + 1];
+  uint16_t unit[kSchedCap];
+};
+
+// How the schedule builder sees unit u: its predicted cost (K/V or Q/dO tile
+// steps plus a fixed per-unit overhead, in steps) and the group of heads whose
+// tiles it streams.  Groups are sized so that the tiles of one group stay
+// resident in L2 (kSchedGroupBytes), and are visited one after another.
+struct SchedUnit {
+  float cost;
+  int group;
+};
+constexpr double kSchedGroupBytes = 32.0 * 1024 * 1024;
+// Heads per group when one head streams `bytes_per_head` bytes.
+int sched_group_heads(double bytes_per_head);
+// Fills *out for `units` units over `workers` workers: units are taken group
+// by group, longest first within a group, and each goes to the worker the
+// costs predict to be free first (list scheduling, LPT order within groups).
+// Results are cached per process under `key` (the launch's shape).  Returns
+// false, with out->workers = 0, when the problem does not fit the table.
+bool build_schedule(const long long (&key)[12], int workers, int units, void (*describe)(const void*, int, SchedUnit*),
+                    const void* ctx, SchedTable* out);
+
+// The table a dense single-CTA forward launch over `workers` workers uses
+// (fa_fwd.cu; for fa_debug_schedule).
+bool fwd_schedule_for(int fp8, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int workers,
+                      SchedTable* sc);
+
+// The same for the backward dQ (kv = 0) or dK/dV (kv = 1) kernel (fa_bwd.cu).
+bool bwd_schedule_for(int kv, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int workers,
+                      SchedTable* sc);
+
 // Forward kernel (fa_fwd.cu); dispatches to the split-KV path itself.
 fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                      int Nq, int Nk, int d, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream,

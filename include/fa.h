@@ -280,6 +280,28 @@ fa_status fa_debug_soft_exp(int on);
  */
 fa_status fa_debug_fwd_pair(int on);
 
+/*
+ * fa_debug_schedule -- the work schedule a persistent launch would use (host
+ * only, enqueues nothing; for tooling and tests).  kernel: 0 the bf16
+ * forward, 1 the 8-bit forward (always the built-in order), 2 the backward
+ * dQ kernel, 3 the backward dK/dV kernel, each for a dense problem of the
+ * given shape over `workers` persistent CTAs (the SM count on the device).
+ *
+ * The kernels' units are independent blocks of rows of one head (the
+ * work decomposition of the FlashAttention pages: per (batch, head) blocks of
+ * query rows, or of keys for dK/dV).  Under a causal mask their costs differ,
+ * so the host orders them: heads are taken in groups whose K/V (or Q/dO)
+ * tiles fit in L2, the longest units of a group first, each to the worker
+ * predicted to be free first.  On return *table_workers is the number of
+ * worker lists (0: no table, the kernel deals its units in its built-in snake
+ * order), start[w] .. start[w+1] (start has table_workers + 1 entries) index
+ * worker w's units in `units`, in the order it runs them.  capacity is the
+ * length of `units`; FA_ERR_SHAPE if it is too small or the shape invalid,
+ * FA_ERR_VALUE for an unknown kernel, FA_ERR_NULL for a null pointer.
+ */
+fa_status fa_debug_schedule(int kernel, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int workers,
+                            int32_t* start, int32_t* units, int capacity, int* table_workers);
+
 /* Dynamic shared memory (bytes) and threads per CTA used for head dim d;
  * 0 for an unsupported d.  For tooling and tests. */
 int fa_fwd_smem_bytes(int d);

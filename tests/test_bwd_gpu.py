@@ -73,6 +73,8 @@ BWD = [
     (1, 4, 1, 512, 512, 128, True),      # MQA, several tiles
     (1, 1, 1, 1, 5, 64, False),          # a single query row
     (2, 3, 3, 257, 129, 64, False),      # ragged d = 64
+    (2, 16, 16, 1300, 1300, 64, True),   # more units than SMs in both kernels: host-built worker lists
+    (1, 24, 6, 1000, 1500, 128, True),   # the same for the dQ kernel, GQA, Nq < Nk
 ]
 
 

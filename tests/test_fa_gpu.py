@@ -88,6 +88,24 @@ def test_edge_shapes(fa, dev, shape):
     compare(o, lse, ref_o, ref_lse, str(shape))
 
 
+# More units than SMs: the host-built worker lists (SchedTable) run them.
+SCHEDULED = [
+    (3, 20, 5, 1000, 1300, 128, True),   # GQA, Nq < Nk, ragged
+    (2, 40, 40, 700, 700, 64, False),
+    (2, 24, 8, 1500, 900, 128, True),    # Nq > Nk: early rows see no key
+]
+
+
+@pytest.mark.parametrize("shape", SCHEDULED, ids=["-".join(map(str, s)) for s in SCHEDULED])
+def test_scheduled_shapes(fa, dev, shape):
+    B, Hq, Hkv, Nq, Nk, d, causal = shape
+    assert fa.fa_debug_schedule(0, B, Hq, Hkv, Nq, Nk, d, causal, torch.cuda.get_device_properties(dev)
+                                .multi_processor_count) is not None
+    prob = make_dense(B, Hq, Hkv, Nq, Nk, d, seed=sum(shape) + 11, causal=causal, name="scheduled")
+    o, lse = run_gpu(fa, prob, dev, keep_on_device=True)
+    compare_per_head(o, lse, prob)
+
+
 VARLEN = [
     ([1, 127, 128, 129, 0, 300, 256, 257], 4, 2, 64, True),
     ([1, 127, 128, 129, 0, 300, 256, 257], 4, 2, 128, False),

@@ -78,6 +78,7 @@ FP8 = [
     (1, 2, 2, 400, 208, True),      # Nq > Nk: early rows see no key
     (1, 2, 1, 64, 16, False),       # one short K/V tile
     (1, 8, 1, 640, 640, True),      # MQA, several units
+    (3, 20, 5, 700, 1008, True),    # more units than SMs, GQA, Nq < Nk
 ]
 
 
@@ -127,6 +128,7 @@ FP8_D64 = [
     (2, 4, 2, 300, 304, True),
     (1, 2, 2, 400, 208, True),
     (1, 8, 1, 640, 640, True),
+    (2, 40, 8, 700, 704, False),    # more units than SMs
 ]
 
 
