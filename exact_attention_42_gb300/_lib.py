@@ -23,6 +23,12 @@ class FaError(RuntimeError):
         super().__init__("%s failed: %s" % (what, fa_status_string(status)))
 
 
+def lib_path() -> str:
+    """The library this process loads: libfa.so, or the one FA_LIBRARY names
+    (the debug build's tests point it at libfa_debug.so)."""
+    return os.environ.get("FA_LIBRARY") or LIB_PATH
+
+
 def lib() -> ctypes.CDLL:
     """The loaded library; raises if it has not been built."""
     global _lib
@@ -30,10 +36,10 @@ def lib() -> ctypes.CDLL:
         return _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise RuntimeError("libfa.so is not built (%s); run exact_attention_42_gb300.build.build()"
-                                   % LIB_PATH)
-            L = ctypes.CDLL(LIB_PATH)
+            path = lib_path()
+            if not os.path.exists(path):
+                raise RuntimeError("%s is not built; run exact_attention_42_gb300.build.build()" % path)
+            L = ctypes.CDLL(path)
             vp, ci = ctypes.c_void_p, ctypes.c_int
             L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ctypes.c_float, ci, vp, vp]
             L.fa_fwd.restype = ci

@@ -5,12 +5,33 @@ the attention computation runs in the library's CUDA kernel.
 """
 from __future__ import annotations
 
+import functools
 import math
+import os
 from typing import Optional, Tuple
 
 import torch
 
 from ._lib import FaError, fa_bwd, fa_fp8_quantize, fa_fwd, fa_fwd_fp8
+
+# NVTX ranges around every entry point, for profilers that show them (ncu's
+# --nvtx filters, for one): on when FA_NVTX is set to a non-zero value.
+NVTX = os.environ.get("FA_NVTX", "") not in ("", "0")
+
+
+def _nvtx(name: str):
+    def wrap(fn):
+        @functools.wraps(fn)
+        def call(*args, **kwargs):
+            if not NVTX:
+                return fn(*args, **kwargs)
+            torch.cuda.nvtx.range_push(name)
+            try:
+                return fn(*args, **kwargs)
+            finally:
+                torch.cuda.nvtx.range_pop()
+        return call
+    return wrap
 
 
 def _check(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int, device) -> None:
@@ -26,6 +47,7 @@ def _check(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int, device) ->
         raise ValueError("%s must be contiguous" % name)
 
 
+@_nvtx("fa.fwd")
 def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
         scale: Optional[float] = None, cu_seqlens: Optional[torch.Tensor] = None,
         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
@@ -84,6 +106,7 @@ def fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
     return out, lse
 
 
+@_nvtx("fa.fwd_host")
 def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
              scale: Optional[float] = None, cu_seqlens: Optional[torch.Tensor] = None,
              device: Optional[torch.device] = None, out: Optional[torch.Tensor] = None,
@@ -151,6 +174,7 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
     return out, lse
 
 
+@_nvtx("fa.bwd")
 def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse: torch.Tensor,
         dout: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
         stream: Optional[torch.cuda.Stream] = None, dq: Optional[torch.Tensor] = None,
@@ -213,6 +237,7 @@ def bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, o: torch.Tensor, lse:
     return dq, dk, dv, delta
 
 
+@_nvtx("fa.fwd_fp8")
 def fwd_fp8(q8: torch.Tensor, k8: torch.Tensor, vt8: torch.Tensor, q_descale: torch.Tensor,
             k_descale: torch.Tensor, v_descale: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
@@ -282,6 +307,7 @@ def hadamard_signs(d: int, seed: int, device=None) -> torch.Tensor:
     return s.to(device) if device is not None else s
 
 
+@_nvtx("fa.fp8_quantize")
 def fp8_quantize(x: torch.Tensor, signs: Optional[torch.Tensor] = None, transpose: bool = False,
                  out: Optional[torch.Tensor] = None, descale: Optional[torch.Tensor] = None,
                  stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
@@ -325,6 +351,7 @@ def fp8_quantize(x: torch.Tensor, signs: Optional[torch.Tensor] = None, transpos
     return out, descale
 
 
+@_nvtx("fa.fwd_fp8_from_bf16")
 def fwd_fp8_from_bf16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
                       scale: Optional[float] = None, rotate: bool = True, seed: int = 0,
                       stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:

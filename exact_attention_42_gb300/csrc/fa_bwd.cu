@@ -94,8 +94,28 @@ __device__ __forceinline__ constexpr bool soft_pair(int i) {
 __device__ __forceinline__ float2 u2f2(uint32_t a, uint32_t b) { return make_float2(__uint_as_float(a), __uint_as_float(b)); }
 
 // Device status word: bit (1 << role) is set when that role gave up waiting.
-// dQ kernel: 0 producer, 1 MMA, 2 softmax; dK/dV kernel: 4, 5, 6.
+// dQ kernel: 0 producer, 1 MMA, 2 softmax; dK/dV kernel: 4, 5, 6.  Bit
+// DEBUG_BIT: a debug build's address check failed.
 __device__ int g_bwd_status;
+constexpr int DEBUG_BIT = 3;
+
+// Debug builds (FA_DEBUG) check every computed TMA coordinate and output row
+// before use; a failed check sets DEBUG_BIT and skips the access (a skipped
+// copy then ends in the bounded time-out).  Release builds compile them away.
+__device__ __forceinline__ bool dcheck(bool ok) {
+#ifdef FA_DEBUG
+  if (!ok) atomicOr(&g_bwd_status, 1 << DEBUG_BIT);
+  return ok;
+#else
+  (void)ok;
+  (void)DEBUG_BIT;
+  return true;
+#endif
+}
+__device__ __forceinline__ void checked_load(uint32_t dst, const CUtensorMap* map, const MapExtent& e, uint32_t bar,
+                                             int x, int y, int z) {
+  if (dcheck(tma_coords_ok(e, x, y, z))) tma_load_3d(dst, map, bar, x, y, z);
+}
 
 // Shared memory of one kernel: two resident tiles (Q and dO for the dQ
 // kernel, K and V for the dK/dV kernel), a ring of NS streamed tiles and, for
@@ -133,6 +153,8 @@ struct Params {
   const int* cu_seqlens;  // null: dense; else B+1 offsets of packed sequences (Nq == Nk == T)
   unsigned long long wait_limit_ns;
   int fault_inject;       // test hook: 1 = the launched kernel's ring producer withholds its first fill
+  // Extents, for the debug build's checks: tensor-map rows per head and heads.
+  int q_rows, kv_rows, q_heads, kv_heads;
 };
 
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, int role) {
@@ -382,6 +404,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   grid_dependency_wait();
   if (threadIdx.x == 0) grid_launch_dependents();
   const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_tiles(p) * (KV_KERNEL ? p.Hkv : p.Hq);
+  // Map extents for the debug checks (Q and dO share one; K and V another).
+  const MapExtent eq{D, p.q_rows, p.q_heads, 2, 0};
+  const MapExtent ek{D, p.kv_rows, p.kv_heads, 2, 0};
   // Dense problems run the host-built worker lists (SchedTable), packed ones the snake order.
   const bool table = sc.workers == static_cast<int>(gridDim.x) && p.cu_seqlens == nullptr;
   const int slot0 = table ? sc.start[blockIdx.x] : 0;
@@ -409,8 +434,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!(ok = wait_or_abort(qempty_bar, (qfills & 1u) ^ 1u, abort_flag, 0, p.wait_limit_ns))) break;
         mbar_arrive_expect_tx(qfull_bar, 2 * C::TILE_BYTES);
         for (int c = 0; c < C::CHUNKS; ++c) {
-          tma_load_3d(smem_u32(sQ) + c * C::CHUNK_BYTES, &tm_q, qfull_bar, c * 64, w.q_y + w.row0, w.q_z);
-          tma_load_3d(smem_u32(sDO) + c * C::CHUNK_BYTES, &tm_do, qfull_bar, c * 64, w.q_y + w.row0, w.q_z);
+          checked_load(smem_u32(sQ) + c * C::CHUNK_BYTES, &tm_q, eq, qfull_bar, c * 64, w.q_y + w.row0, w.q_z);
+          checked_load(smem_u32(sDO) + c * C::CHUNK_BYTES, &tm_do, eq, qfull_bar, c * 64, w.q_y + w.row0, w.q_z);
         }
         ++qfills;
         for (int j = 0; j < nkv && ok; ++j) {
@@ -425,8 +450,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
             const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
             for (int c = 0; c < C::CHUNKS; ++c)
-              tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, full_bar(s), c * 64, w.k_y + j * TILE,
-                          w.k_z);
+              checked_load(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, ek, full_bar(s), c * 64, w.k_y + j * TILE,
+                           w.k_z);
             ++it;
           }
         }
@@ -547,8 +572,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int row = w.row0 + r;
       const bool row_ok = row < w.Lq;
       const long long grow = static_cast<long long>(w.q_z) * p.Nq + w.q_y + row;
+      // Debug build: the row lies inside dQ (q_heads * q_rows rows).
+      const bool grow_ok = !row_ok || dcheck(grow >= 0 && grow < static_cast<long long>(p.q_heads) * p.q_rows);
       if (nkv == 0) {
-        if (row_ok) {
+        if (row_ok && grow_ok) {
           uint4* dst = reinterpret_cast<uint4*>(p.dq + grow * D + (D / 2) * h);
 #pragma unroll
           for (int i = 0; i < D / 16; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -629,7 +656,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           out[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * p.scale, __uint_as_float(raw[2 * i + 1]) * p.scale);
-        if (row_ok) {
+        if (row_ok && grow_ok) {
           uint4* dst = reinterpret_cast<uint4*>(p.dq + grow * D + (D / 2) * h + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
@@ -783,6 +810,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   grid_dependency_wait();
   if (threadIdx.x == 0) grid_launch_dependents();
   const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_tiles(p) * (KV_KERNEL ? p.Hkv : p.Hq);
+  // Map extents for the debug checks (Q and dO share one; K and V another).
+  const MapExtent eq{D, p.q_rows, p.q_heads, 2, 0};
+  const MapExtent ek{D, p.kv_rows, p.kv_heads, 2, 0};
   // Dense problems run the host-built worker lists (SchedTable), packed ones the snake order.
   const bool table = sc.workers == static_cast<int>(gridDim.x) && p.cu_seqlens == nullptr;
   const int slot0 = table ? sc.start[blockIdx.x] : 0;
@@ -808,8 +838,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!(ok = wait_or_abort(kvempty_bar, (kvfills & 1u) ^ 1u, abort_flag, 4, p.wait_limit_ns))) break;
         mbar_arrive_expect_tx(kvfull_bar, 2 * C::TILE_BYTES);
         for (int c = 0; c < C::CHUNKS; ++c) {
-          tma_load_3d(smem_u32(sK) + c * C::CHUNK_BYTES, &tm_k, kvfull_bar, c * 64, w.k_y + w.key0, w.k_z);
-          tma_load_3d(smem_u32(sV) + c * C::CHUNK_BYTES, &tm_v, kvfull_bar, c * 64, w.k_y + w.key0, w.k_z);
+          checked_load(smem_u32(sK) + c * C::CHUNK_BYTES, &tm_k, ek, kvfull_bar, c * 64, w.k_y + w.key0, w.k_z);
+          checked_load(smem_u32(sV) + c * C::CHUNK_BYTES, &tm_v, ek, kvfull_bar, c * 64, w.k_y + w.key0, w.k_z);
         }
         ++kvfills;
         for (int hg = 0; hg < p.group && ok; ++hg) {
@@ -826,8 +856,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
               const uint32_t dst = smem_u32(sRing + s * C::TILE_BYTES);
               for (int c = 0; c < C::CHUNKS; ++c)
-                tma_load_3d(dst + c * C::CHUNK_BYTES, x ? &tm_do : &tm_q, full_bar(s), c * 64, w.q_y + i * TILE,
-                            qz);
+                checked_load(dst + c * C::CHUNK_BYTES, x ? &tm_do : &tm_q, eq, full_bar(s), c * 64, w.q_y + i * TILE,
+                             qz);
               ++it;
             }
           }
@@ -959,8 +989,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int key = w.key0 + r;
       const bool key_ok = key < w.Lk;
       const long long krow = static_cast<long long>(w.k_z) * p.Nk + w.k_y + key;
+      // Debug build: the row lies inside dK and dV (kv_heads * kv_rows rows).
+      const bool krow_ok = !key_ok || dcheck(krow >= 0 && krow < static_cast<long long>(p.kv_heads) * p.kv_rows);
       if (i0 >= nq) {
-        if (key_ok) {
+        if (key_ok && krow_ok) {
           uint4* dk = reinterpret_cast<uint4*>(p.dk + krow * D + (D / 2) * h);
           uint4* dv = reinterpret_cast<uint4*>(p.dv + krow * D + (D / 2) * h);
 #pragma unroll
@@ -1087,7 +1119,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             out[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * mul, __uint_as_float(raw[2 * i + 1]) * mul);
-          if (key_ok) {
+          if (key_ok && krow_ok) {
             uint4* dst = reinterpret_cast<uint4*>(base + c0);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -1260,6 +1292,10 @@ static fa_status launch_bwd_t(const void* q, const void* k, const void* v, const
   prm.nkt = (Nk + bwd::TILE - 1) / bwd::TILE;
   prm.wait_limit_ns = wait_limit_ns;
   prm.cu_seqlens = cu_seqlens;
+  prm.q_rows = Nq;
+  prm.kv_rows = Nk;
+  prm.q_heads = static_cast<int>(q_heads);
+  prm.kv_heads = static_cast<int>(kv_heads);
   // Packed: the units are counted on the device; every sequence adds at most
   // one partial tile, which bounds the grid.
   const long long tiles_bound = packed ? (Nq + bwd::TILE - 1) / bwd::TILE + B : 0;

@@ -116,8 +116,25 @@ static_assert(P_PARTS == 1 || P_PARTS == 2 || P_PARTS == 4, "P_PARTS divides the
 // the parity tests cover it as fully as possible.
 constexpr int SOFT_EXP_PERIOD = 2;
 
-// Device status word: bit (1 << role) is set when that role gave up waiting.
+// Device status word: bit (1 << role) is set when that role gave up waiting;
+// bit DEBUG_BIT when a debug build's address check failed.
 __device__ int g_fa_status;
+constexpr int DEBUG_BIT = 5;
+
+// Debug builds (FA_DEBUG) check every computed TMA coordinate, output row
+// and TMEM base column before use.  A failed check sets DEBUG_BIT and the
+// access is skipped (a skipped copy then ends in the bounded time-out); it
+// never traps.  Release builds compile the checks away.
+__device__ __forceinline__ bool dcheck(bool ok) {
+#ifdef FA_DEBUG
+  if (!ok) atomicOr(&g_fa_status, 1 << DEBUG_BIT);
+  return ok;
+#else
+  (void)ok;
+  (void)DEBUG_BIT;
+  return true;
+#endif
+}
 
 // FP8 selects the 8-bit path: e4m3 Q, K and V^T, products of kind f8f6f4.
 // PAIR selects the CTA-pair path: two CTAs of a cluster share each product
@@ -171,7 +188,23 @@ struct Params {
   const float* q_descale;
   const float* k_descale;
   const float* v_descale;
+  // Extents, for the debug build's checks: rows per head of the Q and K/V
+  // tensor maps, their head counts, and the rows of O and LSE.
+  int q_rows, kv_rows, q_heads, kv_heads;
+  long long o_rows;
 };
+
+__device__ __forceinline__ void checked_load(uint32_t dst, const CUtensorMap* map, const MapExtent& e, uint32_t bar,
+                                             int x, int y, int z) {
+  if (dcheck(tma_coords_ok(e, x, y, z))) tma_load_3d(dst, map, bar, x, y, z);
+}
+__device__ __forceinline__ void checked_load_pair(uint32_t dst, const CUtensorMap* map, const MapExtent& e,
+                                                  uint32_t bar, int x, int y, int z) {
+  if (dcheck(tma_coords_ok(e, x, y, z))) tma_load_3d_pair(dst, map, bar, x, y, z);
+}
+__device__ __forceinline__ void checked_prefetch(const CUtensorMap* map, const MapExtent& e, int x, int y, int z) {
+  if (dcheck(tma_coords_ok(e, x, y, z))) tma_prefetch_l2_3d(map, x, y, z);
+}
 
 struct Unit {
   int Lq, Lk;        // sequence lengths (queries, keys)
@@ -412,6 +445,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // next kernel may then start its own set-up on the SMs this grid frees.
   grid_dependency_wait();
   if (threadIdx.x == 0) grid_launch_dependents();
+  // Map extents for the debug checks.  On the pair path a CTA whose rows lie
+  // past the sequence end still loads its (all-fill) Q box, and the odd CTA's
+  // half of the last K tile (keys [64, 128)) may start past the last key.
+  const MapExtent eq{D, p.q_rows, p.q_heads, C::ELEM, PAIR ? BLOCK_M : 0};
+  const MapExtent ek{D, p.kv_rows, p.kv_heads, C::ELEM, PAIR ? BLOCK_N / 2 : 0};
+  const MapExtent ev = FP8 ? MapExtent{p.kv_rows, D, p.kv_heads, 1, 0} : ek;  // 8-bit: V^T, keys along x
 
   const int num_units = (p.cu_seqlens == nullptr) ? p.num_units : packed_num_units(p, C::UNIT_ROWS);
   // Static "snake" schedule over the grid's G persistent workers (CTAs, or
@@ -457,21 +496,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int t = 0; t < NQT; ++t) {
           if ((t == 0 ? nk0 : nk1) == 0) continue;
           for (int c = 0; c < C::CHUNKS; ++c)
-            tma_prefetch_l2_3d(&tm_q, c * C::CHUNK_COLS, wn.q_y + wn.row0 + t * C::TILE_ROWS + rank * BLOCK_M,
+            checked_prefetch(&tm_q, eq, c * C::CHUNK_COLS, wn.q_y + wn.row0 + t * C::TILE_ROWS + rank * BLOCK_M,
                                wn.q_z);
         }
         const int nn = min(max(nk0, nk1), PREFETCH_KV_TILES);
         for (int j = 0; j < nn; ++j)
           for (int c = 0; c < C::CHUNKS; ++c) {
             if constexpr (PAIR) {  // this CTA's halves: keys [64 rank, +64) of K, columns [64 rank, +64) of V
-              tma_prefetch_l2_3d(&tm_k, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N + rank * (BLOCK_N / 2), wn.k_z);
-              if (c == 0) tma_prefetch_l2_3d(&tm_v, rank * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
+              checked_prefetch(&tm_k, ek, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N + rank * (BLOCK_N / 2), wn.k_z);
+              if (c == 0) checked_prefetch(&tm_v, ev, rank * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
             } else {
-              tma_prefetch_l2_3d(&tm_k, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
+              checked_prefetch(&tm_k, ek, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
               if constexpr (FP8)  // V^T: keys along x, head dims along y
-                tma_prefetch_l2_3d(&tm_v, wn.k_y + j * BLOCK_N, 0, wn.k_z);
+                checked_prefetch(&tm_v, ev, wn.k_y + j * BLOCK_N, 0, wn.k_z);
               else
-                tma_prefetch_l2_3d(&tm_v, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
+                checked_prefetch(&tm_v, ev, c * C::CHUNK_COLS, wn.k_y + j * BLOCK_N, wn.k_z);
             }
           }
       };
@@ -499,19 +538,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * C::SLOT_BYTES);
               if (kv == 0) {  // K: keys [64 rank, +64) of the tile, every head dim
                 for (int c = 0; c < C::CHUNKS; ++c)
-                  tma_load_3d_pair(dst + c * (C::SLOT_BYTES / C::CHUNKS), &tm_k, fb, c * C::CHUNK_COLS,
-                                   w.k_y + j * BLOCK_N + rank * (BLOCK_N / 2), w.k_z);
+                  checked_load_pair(dst + c * (C::SLOT_BYTES / C::CHUNKS), &tm_k, ek, fb, c * C::CHUNK_COLS,
+                                    w.k_y + j * BLOCK_N + rank * (BLOCK_N / 2), w.k_z);
               } else {        // V: head dims [64 rank, +64) of every key of the tile
-                tma_load_3d_pair(dst, &tm_v, fb, rank * C::CHUNK_COLS, w.k_y + j * BLOCK_N, w.k_z);
+                checked_load_pair(dst, &tm_v, ev, fb, rank * C::CHUNK_COLS, w.k_y + j * BLOCK_N, w.k_z);
               }
             } else {
               mbar_arrive_expect_tx(full_bar(s), C::TILE_BYTES);
               if (FP8 && kv) {  // V^T tile: 128 head dims (rows) x 128 keys (bytes)
-                tma_load_3d(dst, &tm_v, full_bar(s), w.k_y + j * BLOCK_N, 0, w.k_z);
+                checked_load(dst, &tm_v, ev, full_bar(s), w.k_y + j * BLOCK_N, 0, w.k_z);
               } else {
                 for (int c = 0; c < C::CHUNKS; ++c)
-                  tma_load_3d(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, full_bar(s), c * C::CHUNK_COLS,
-                              w.k_y + j * BLOCK_N, w.k_z);
+                  checked_load(dst + c * C::CHUNK_BYTES, kv ? &tm_v : &tm_k, kv ? ev : ek, full_bar(s),
+                               c * C::CHUNK_COLS, w.k_y + j * BLOCK_N, w.k_z);
               }
             }
             ++it;
@@ -549,12 +588,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if constexpr (PAIR) {
             if (rank == 0) mbar_arrive_expect_tx(qfull_bar(t), 2 * C::TILE_BYTES);
             for (int c = 0; c < C::CHUNKS; ++c)
-              tma_load_3d_pair(dst + c * C::CHUNK_BYTES, &tm_q, leader_bar(qfull_bar(t)), c * C::CHUNK_COLS, row,
-                               w.q_z);
+              checked_load_pair(dst + c * C::CHUNK_BYTES, &tm_q, eq, leader_bar(qfull_bar(t)), c * C::CHUNK_COLS,
+                                row, w.q_z);
           } else {
             mbar_arrive_expect_tx(qfull_bar(t), C::TILE_BYTES);
             for (int c = 0; c < C::CHUNKS; ++c)
-              tma_load_3d(dst + c * C::CHUNK_BYTES, &tm_q, qfull_bar(t), c * C::CHUNK_COLS, row, w.q_z);
+              checked_load(dst + c * C::CHUNK_BYTES, &tm_q, eq, qfull_bar(t), c * C::CHUNK_COLS, row, w.q_z);
           }
           ++qfills[t];
         }
@@ -743,6 +782,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp % 4) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
     const uint32_t tO = tmem + lane_base + 256 + t * 128;
+    // Debug build: this thread's S and O columns lie inside the 512 allocated.
+    dcheck(((tS & 0xFFFFu) - (tmem & 0xFFFFu)) + BLOCK_N <= 512u && ((tO & 0xFFFFu) - (tmem & 0xFFFFu)) + D <= 512u &&
+           (tS >> 16) == static_cast<uint32_t>((warp % 4) * 32));
     const float sl2_base = p.scale_log2;
     const float NEG_INF = -INFINITY;
     constexpr float tau = FP8 ? TAU_FP8 : TAU;
@@ -923,13 +965,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pk[i] = pack_bf16x2(__uint_as_float(raw[2 * i]) * inv_l, __uint_as_float(raw[2 * i + 1]) * inv_l);
-        if (row_ok) {
+        if (row_ok && dcheck(w.out_row + row >= 0 && w.out_row + row < p.o_rows)) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
-      if (row_ok) {
+      if (row_ok && dcheck(w.out_row + row >= 0 && w.out_row + row < p.o_rows)) {
         const float lse = (l > 0.f) ? (m_used - p_shift + __log2f(l)) * 0.69314718055994531f : NEG_INF;
         p.lse[w.out_row + row] = lse;
       }
@@ -1099,6 +1141,16 @@ static void fwd_schedule(SchedTable* sc, int kind, int B, int Hq, int Hkv, int N
   build_schedule(key, static_cast<int>(grid), static_cast<int>(units), describe_fwd_unit, &c, sc);
 }
 
+// Tensor extents for the debug build's checks (tensor-map heads: (batch,
+// head) pairs, or heads alone when packed).
+static void set_extents(Params& prm, long long q_heads, long long kv_heads) {
+  prm.q_rows = prm.Nq;
+  prm.kv_rows = prm.Nk;
+  prm.q_heads = static_cast<int>(q_heads);
+  prm.kv_heads = static_cast<int>(kv_heads);
+  prm.o_rows = q_heads * prm.Nq;
+}
+
 template <int D>
 static fa_status launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                         int Nq, int Nk, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream,
@@ -1152,6 +1204,7 @@ static fa_status launch(const void* q, const void* k, const void* v, void* o, fl
   prm.fault_inject = env.fault_mode == kFaultFwd ? 1 : 0;
   prm.key_align = 1;
   prm.q_descale = prm.k_descale = prm.v_descale = nullptr;
+  set_extents(prm, q_heads, kv_heads);
   long long grid;  // persistent workers: CTAs, or CTA pairs
   if (packed) {
     prm.nqb = 0;
@@ -1244,6 +1297,7 @@ static fa_status launch_fp8(const void* q8, const void* k8, const void* vt8, con
   prm.q_descale = q_descale;
   prm.k_descale = k_descale;
   prm.v_descale = v_descale;
+  set_extents(prm, q_heads, kv_heads);
   long long grid;
   if (packed) {
     prm.nqb = 0;

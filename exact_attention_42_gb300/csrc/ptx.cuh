@@ -419,6 +419,20 @@ __device__ __forceinline__ void tmem_wait_st() {
 #undef FA_R8
 #undef FA_W8
 
+// Extent of one 3-D tensor map, for the debug checks: `cols` elements of
+// `elem` bytes per row, `rows` rows per head, `heads` heads.  `row_slack`
+// admits boxes that start that many rows past the end (all fill).
+struct MapExtent {
+  int cols, rows, heads, elem, row_slack;
+};
+
+// A TMA box at (x, y, z): x must sit on a 16-byte boundary, and the box must
+// start inside the tensor.
+__device__ __forceinline__ bool tma_coords_ok(const MapExtent& e, int x, int y, int z) {
+  return x >= 0 && x < e.cols && (x * e.elem) % 16 == 0 && y >= 0 && y < e.rows + e.row_slack && z >= 0 &&
+         z < e.heads;
+}
+
 // ---------------------------------------------------------------------------
 // Register reallocation between warpgroups (every thread of a warpgroup must
 // execute the same instruction).  The sum over warps after the change must

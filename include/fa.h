@@ -216,7 +216,14 @@ const char* fa_status_string(fa_status s);
  * (K/V producer, MMA issuer, softmax of query tiles 0 and 1, Q loader);
  * bit 8: the split-KV kernel; bits 9-11 and 13-15: producer, MMA issuer and
  * softmax roles of fa_bwd's dQ and dK/dV kernels; bit 16: fa_fp8_quantize's
- * one-launch kernel.  Returns FA_OK and stores
+ * one-launch kernel.  In a library compiled with FA_DEBUG (libfa_debug.so,
+ * built by the package's build(debug=True)), the fa_fwd / fa_fwd_fp8 kernel
+ * and fa_bwd's dQ and dK/dV kernels check every TMA box they request (the
+ * x coordinate on a 16-byte boundary, the box starting inside the tensor),
+ * every output row they write and their TMEM columns before use; a failed
+ * check sets bit 5 (forward) or bit 12 (backward) and the access is skipped.
+ * Release builds compile the checks away and never set those bits.
+ * Returns FA_OK and stores
  * 0 in *bits when nothing went wrong, FA_ERR_TIMEOUT with the bits otherwise.
  * The call first waits for all work on the current device (every stream,
  * cudaDeviceSynchronize), so no kernel can set a bit between the read and the
