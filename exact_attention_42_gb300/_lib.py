@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L.fa_bwd_smem_bytes.restype = ci
             L.fa_fp8_quantize.argtypes = [vp, vp, vp, ci, ci, ci, ci, ci, vp, vp]
             L.fa_fp8_quantize.restype = ci
+            L.fa_fwd_host.argtypes = [vp] * 10 + [ci] * 6 + [ctypes.c_float, ci, vp, vp, ci, vp]
+            L.fa_fwd_host.restype = ci
             L.fa_debug_schedule.argtypes = [ci] * 9 + [vp, vp, ci, ctypes.POINTER(ci)]
             L.fa_debug_schedule.restype = ci
             _lib = L
@@ -82,6 +84,13 @@ def fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, cu_seqlens, st
     """Direct call of the C entry point with integer addresses; returns the status."""
     return lib().fa_fwd(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, ctypes.c_float(scale), int(causal),
                         cu_seqlens, stream)
+
+
+def fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d, B, Hq, Hkv, Nq, Nk, d, scale, causal,
+                cu_h, cu_d, pieces, stream) -> int:
+    """Direct call of the host-buffer forward with integer addresses; returns the status."""
+    return lib().fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d, B, Hq, Hkv, Nq, Nk, d,
+                             ctypes.c_float(scale), int(causal), cu_h, cu_d, int(pieces), stream)
 
 
 def fa_decode(q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, stream) -> int:

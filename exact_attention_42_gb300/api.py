@@ -12,7 +12,7 @@ from typing import Optional, Tuple
 
 import torch
 
-from ._lib import FaError, fa_bwd, fa_fp8_quantize, fa_fwd, fa_fwd_fp8
+from ._lib import FaError, fa_bwd, fa_fp8_quantize, fa_fwd, fa_fwd_fp8, fa_fwd_host
 
 # NVTX ranges around every entry point, for profilers that show them (ncu's
 # --nvtx filters, for one): on when FA_NVTX is set to a non-zero value.
@@ -111,66 +111,67 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
              scale: Optional[float] = None, cu_seqlens: Optional[torch.Tensor] = None,
              device: Optional[torch.device] = None, out: Optional[torch.Tensor] = None,
              lse: Optional[torch.Tensor] = None, chunks: int = 4) -> Tuple[torch.Tensor, torch.Tensor]:
-    """The forward for host tensors: copies the inputs to the GPU, runs the
-    kernel, copies O and LSE back to host memory and waits for the result.
+    """The forward for host tensors, through the C entry fa_fwd_host: copies
+    the inputs to the GPU, runs the kernel, copies O and LSE back to host
+    memory and waits for the result.
 
     Dense inputs are processed in about ``chunks`` pieces, each a contiguous
-    (batch, key/value head range) slice with its query heads.  Input copies,
-    kernels and output copies run on three streams, so the copies of one
-    piece overlap the kernel and the copies of others.  (On GB300 the
-    host-to-device copies of the B2/H32/N4096 inputs then bound the call.)  Inputs in pinned
-    memory make the copies asynchronous; ``out`` / ``lse`` (host tensors of
-    O's and LSE's shapes, pinned for overlap) receive the results, otherwise
-    they are allocated, pinned when the inputs are.  Packed batches, or
-    chunks <= 1, take one piece.
+    (batch, key/value head range) slice with its query heads; the library
+    overlaps one piece's copies with the kernel and the copies of others (on
+    GB300 the host-to-device copies of the B2/H32/N4096 inputs then bound the
+    call).  Inputs in pinned memory make the copies asynchronous; ``out`` /
+    ``lse`` (host tensors of O's and LSE's shapes, pinned for overlap) receive
+    the results, otherwise they are allocated, pinned when the inputs are.
+    Packed batches (``cu_seqlens`` int32 on the host) take one piece.  The
+    device staging buffers are allocated here, through PyTorch.
     """
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    packed = cu_seqlens is not None
+    nd = 3 if packed else 4
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.dim() != nd or t.is_cuda \
+                or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous bf16 host tensor with %d dims" % (name, nd))
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    if packed:
+        if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.is_cuda:
+            raise ValueError("cu_seqlens must be an int32 host tensor")
+        cu_seqlens = cu_seqlens.contiguous()
+        Hq, Nq, d = q.shape
+        Hkv, Nk, _ = k.shape
+        B = cu_seqlens.numel() - 1
+    else:
+        B, Hq, Nq, d = q.shape
+        _, Hkv, Nk, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
     nb = q.is_pinned()
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, pin_memory=nb)
     if lse is None:
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, pin_memory=nb)
-    if cu_seqlens is not None or chunks <= 1 or q.dim() != 4:
-        qd, kd, vd = (t.to(device, non_blocking=nb) for t in (q, k, v))
-        cud = None if cu_seqlens is None else cu_seqlens.to(device, non_blocking=nb)
-        o, l = fwd(qd, kd, vd, causal=causal, scale=scale, cu_seqlens=cud)
-        out.copy_(o, non_blocking=nb)
-        lse.copy_(l, non_blocking=nb)
-        torch.cuda.current_stream(device).synchronize()
-        return out, lse
-    B, Hq, Nq, d = q.shape
-    Hkv = k.shape[1]
-    g = Hq // Hkv if Hkv > 0 else 1
-    per_b = max(1, -(-chunks // max(B, 1)))          # pieces per batch entry
-    kv_step = max(1, -(-Hkv // per_b))                # key/value heads per piece
-    pieces = [(b, h0, min(Hkv, h0 + kv_step)) for b in range(B) for h0 in range(0, Hkv, kv_step)]
+    if tuple(out.shape) != tuple(q.shape) or out.dtype != torch.bfloat16 or out.is_cuda or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 host tensor shaped like q")
+    if tuple(lse.shape) != tuple(q.shape[:-1]) or lse.dtype != torch.float32 or lse.is_cuda \
+            or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 host tensor of q's leading shape")
     with torch.cuda.device(device):
-        comp = torch.cuda.current_stream(device)
-        s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-        s_in.wait_stream(comp)
         qd = torch.empty(q.shape, dtype=q.dtype, device=device)
         kd = torch.empty(k.shape, dtype=k.dtype, device=device)
         vd = torch.empty(v.shape, dtype=v.dtype, device=device)
         od = torch.empty(q.shape, dtype=q.dtype, device=device)
         ld = torch.empty(q.shape[:-1], dtype=torch.float32, device=device)
-        for b, h0, h1 in pieces:
-            qs, ks = (slice(b, b + 1), slice(h0 * g, h1 * g)), (slice(b, b + 1), slice(h0, h1))
-            with torch.cuda.stream(s_in):
-                qd[qs].copy_(q[qs], non_blocking=nb)
-                kd[ks].copy_(k[ks], non_blocking=nb)
-                vd[ks].copy_(v[ks], non_blocking=nb)
-                ready = torch.cuda.Event()
-                ready.record(s_in)
-            comp.wait_event(ready)
-            fwd(qd[qs], kd[ks], vd[ks], causal=causal, scale=scale, out=od[qs], lse=ld[qs], stream=comp)
-            done = torch.cuda.Event()
-            done.record(comp)
-            s_out.wait_event(done)
-            with torch.cuda.stream(s_out):
-                out[qs].copy_(od[qs], non_blocking=nb)
-                lse[qs].copy_(ld[qs], non_blocking=nb)
-        s_out.synchronize()
-        comp.synchronize()
+        cud = torch.empty(cu_seqlens.shape, dtype=torch.int32, device=device) if packed else None
+        s = torch.cuda.current_stream(device)
+        st = fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                         qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), ld.data_ptr(),
+                         B, Hq, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                         cu_seqlens.data_ptr() if packed else None, cud.data_ptr() if packed else None,
+                         max(1, int(chunks)), s.cuda_stream)
+        if st != 0:
+            raise FaError(st, "fa_fwd_host")
+        s.synchronize()
     return out, lse
 
 

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libfa.so")
 # output row and TMEM base column is checked before use (see include/fa.h).
 DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libfa_debug.so")
 SOURCES = [os.path.join(CSRC, n)
-           for n in ("fa_api.cu", "fa_fwd.cu", "fa_decode.cu", "fa_bwd.cu", "fa_quant.cu", "fa_sched.cu")]
+           for n in ("fa_api.cu", "fa_fwd.cu", "fa_decode.cu", "fa_bwd.cu", "fa_quant.cu", "fa_sched.cu", "fa_host.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, "ptx.cuh"), os.path.join(CSRC, "fa_internal.h"), os.path.join(INCLUDE, "fa.h")]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

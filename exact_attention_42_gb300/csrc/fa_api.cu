@@ -58,6 +58,11 @@ static fa_status launch_env(LaunchEnv* env) {
   return FA_OK;
 }
 
+fa_status check_device() {
+  LaunchEnv env;
+  return launch_env(&env);
+}
+
 }  // namespace fa
 
 extern "C" {

@@ -101,6 +101,10 @@ bool fwd_schedule_for(int fp8, int B, int Hq, int Hkv, int Nq, int Nk, int d, in
 bool bwd_schedule_for(int kv, int B, int Hq, int Hkv, int Nq, int Nk, int d, int causal, int workers,
                       SchedTable* sc);
 
+// FA_OK if the current device is supported (sm_103), FA_ERR_UNSUPPORTED
+// otherwise, FA_ERR_CUDA if it cannot be queried (fa_api.cu).
+fa_status check_device();
+
 // Forward kernel (fa_fwd.cu); dispatches to the split-KV path itself.
 fa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                      int Nq, int Nk, int d, float scale, int causal, const int32_t* cu_seqlens, cudaStream_t stream,

@@ -206,6 +206,40 @@ fa_status fa_fwd_fp8(const void* q8, const void* k8, const void* vt8, const floa
 fa_status fa_fp8_quantize(const void* x, void* x8, float* descale, int B, int H, int N, int d, int transpose,
                           const int8_t* signs, cudaStream_t stream);
 
+/*
+ * fa_fwd_host -- fa_fwd for inputs and outputs in host memory.
+ *
+ * q_h, k_h, v_h, o_h, lse_h: host buffers in fa_fwd's layouts (dense or
+ * packed); pinned (page-locked) memory makes the copies asynchronous and lets
+ * them overlap the kernels.  q_d, k_d, v_d, o_d, lse_d: device buffers of the
+ * same sizes that the caller provides as staging (the library allocates no
+ * device memory); cu_seqlens_h / cu_seqlens_d: the packed offsets on the host
+ * and B+1 int32 of device staging for them (both NULL for a dense problem).
+ *
+ * A dense problem is cut into about `pieces` (>= 1) slices, each one batch
+ * entry with a range of key/value heads and their query heads: contiguous in
+ * every tensor.  Each slice's host-to-device copies run on a copy-in stream,
+ * its fa_fwd launch on `stream` and its device-to-host copies on a copy-out
+ * stream (both copy streams belong to the library, one pair per device), so
+ * the copies of one slice overlap the kernel and the copies of others.  A
+ * packed batch is one slice.  Interview canvas, element flash-text: the
+ * method moves data in tiles between the slow and the fast memory; here the
+ * same idea overlaps the host link with the kernel.
+ *
+ * Asynchronous like fa_fwd: the call returns once everything is enqueued,
+ * and work enqueued on `stream` afterwards sees O and LSE in host memory
+ * (synchronise `stream` before reading them).  The call waits (on the device)
+ * for earlier work on `stream` before it writes the staging buffers.
+ * Errors: fa_fwd's argument errors, plus FA_ERR_SHAPE for pieces < 1 and
+ * FA_ERR_NULL for a missing host or staging buffer, are reported before
+ * anything is enqueued; FA_ERR_CUDA if a copy, stream or event call fails
+ * (copies already enqueued then still run).
+ */
+fa_status fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
+                      void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d,
+                      int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                      const int32_t* cu_seqlens_h, int32_t* cu_seqlens_d, int pieces, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* fa_status_string(fa_status s);
 

@@ -208,6 +208,28 @@ def test_host_entry_matches_device_entry(fa, dev):
     assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
 
 
+@pytest.mark.parametrize("chunks", [1, 3, 7])
+def test_host_entry_pieces_gqa(fa, dev, chunks):
+    # fa_fwd_host cuts a dense problem into (batch, key/value head range)
+    # slices; uneven slices must give the device entry's result bit for bit.
+    prob = make_dense(2, 12, 3, 300, 500, 128, seed=14, causal=True)
+    qh, kh, vh = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (prob.q, prob.k, prob.v))
+    o_h, l_h = fa.fwd_host(qh, kh, vh, causal=True, chunks=chunks)
+    o_d, l_d = fa.fwd(qh.to(dev), kh.to(dev), vh.to(dev), causal=True)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+
+
+def test_host_entry_packed(fa, dev):
+    prob = make_varlen([5, 300, 129, 0, 64], 4, 2, 64, seed=15, causal=True)
+    qh, kh, vh = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (prob.q, prob.k, prob.v))
+    cu = torch.from_numpy(prob.cu_seqlens)
+    o_h, l_h = fa.fwd_host(qh, kh, vh, causal=True, cu_seqlens=cu)
+    o_d, l_d = fa.fwd(qh.to(dev), kh.to(dev), vh.to(dev), causal=True, cu_seqlens=cu.to(dev))
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+    ref_o, ref_lse = oracle_full(prob)
+    compare(o_h.float().numpy().astype(np.float64), l_h.numpy().astype(np.float64), ref_o, ref_lse, "packed host")
+
+
 def test_software_exp2_error_bound(fa, dev):
     """The FMA-pipe 2^x used for part of the exponentials: relative error below
     the minimax bound of its polynomial (7.5e-5, a little slack for rounding)."""
