@@ -62,13 +62,13 @@ constexpr int WARP_QLOAD = 11;
 // Register split.  The kernel is launched at 168 registers per thread (the
 // most 12 warps allow: three warps share each sub-partition's 16K registers).
 // The two softmax warpgroups then grow to REG_SOFTMAX and the load/MMA
-// warpgroup shrinks to REG_OTHER: 8*216 + 4*72 = 2016 = 12*168 (the block's
-// pool) and 2*216 + 72 = 504 <= 512 per sub-partition.
+// warpgroup shrinks to REG_OTHER (per instantiation, see Cfg): bf16
+// 8*216 + 4*72 = 2016 = 12*168 (the block's pool), 8-bit 8*224 + 4*56 = 2016;
+// per sub-partition 2*216 + 72 = 504 and 2*224 + 56 = 504 <= 512.  The 8-bit
+// softmax needs more registers (ptxas: 44 bytes of spills at 216, 28 at
+// 224), and 224/56 measured 0.6-0.7% faster there; bf16 compiles without
+// spills at 216/72 and does not gain from 224/56.
 constexpr int REG_LAUNCH = 168;
-constexpr int REG_SOFTMAX = 216;
-constexpr int REG_OTHER = 72;
-static_assert(8 * REG_SOFTMAX + 4 * REG_OTHER <= 12 * REG_LAUNCH, "register split exceeds the launch pool");
-static_assert(2 * REG_SOFTMAX + REG_OTHER <= 512, "register split exceeds a sub-partition");
 // Conditional rescale threshold in log2 units: the running max used for the
 // exponentials is only moved when a new row max exceeds it by more than TAU,
 // so unnormalised probabilities stay below 2^TAU.  O / l is unchanged by the
@@ -165,6 +165,10 @@ struct Cfg {
   static constexpr int CTAS = PAIR ? 2 : 1;            // CTAs sharing one product tile
   static constexpr int TILE_ROWS = CTAS * BLOCK_M;     // query rows of one product tile
   static constexpr int UNIT_ROWS = NQT * TILE_ROWS;    // query rows of one work unit
+  static constexpr int REG_SOFTMAX = FP8 ? 224 : 216;
+  static constexpr int REG_OTHER = FP8 ? 56 : 72;
+  static_assert(8 * REG_SOFTMAX + 4 * REG_OTHER <= 12 * REG_LAUNCH, "register split exceeds the launch pool");
+  static_assert(2 * REG_SOFTMAX + REG_OTHER <= 512, "register split exceeds a sub-partition");
   // barriers: full[NS], empty[NS], q_full[2], q_empty[2], s_full[2], p_full[2], o_done[2], drain
   static constexpr int NUM_BARS = 2 * NS + (4 + P_PARTS) * NQT + 1;
   static constexpr int SMEM_BYTES = 1024 + SMEM_Q + SMEM_RING + NUM_BARS * 8 + 16;
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto tiles_of = [&](const Unit& w, int t) { return kv_tiles(p, w, t, C::TILE_ROWS); };
 
   if (warp >= 8) {
-  setmaxnreg_dec<REG_OTHER>();
+  setmaxnreg_dec<C::REG_OTHER>();
   if (warp == WARP_PRODUCER) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
@@ -775,7 +779,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     wait_drain(drain_bar, 0, ab, 1, p.wait_limit_ns);
   }
   } else {
-    setmaxnreg_inc<REG_SOFTMAX>();
+    setmaxnreg_inc<C::REG_SOFTMAX>();
     // -------------------------------------------------------------- softmax
     const int t = warp / 4;
     const int r = threadIdx.x % 128;
