@@ -18,9 +18,11 @@
  *   - P is rounded to bf16 before the P*V product; all accumulation is fp32.
  *
  * Thread safety: every entry point is reentrant.  The library's state is
- * once-initialised per-device launch settings, three device status words (one
- * each for the forward, split-KV and backward kernels, merged by
- * fa_device_status) and the process-wide settings of the three test hooks
+ * once-initialised per-device launch settings, four device status words (one
+ * each for the forward, split-KV, backward and one-launch quantizer kernels,
+ * merged by fa_device_status), a per-process cache of the host-built work
+ * lists (guarded by a lock), one pair of copy streams per device for
+ * fa_fwd_host, and the process-wide settings of the three test hooks
  * (fa_debug_fault_injection, fa_debug_soft_exp, fa_debug_fwd_pair): a hook
  * call changes every later launch, from any thread.
  */
