@@ -38,7 +38,7 @@ def fwd_units(B, Hq, Hkv, Nq, Nk, causal, rows=256, tile=128):
                 last = min(last, min(q0 + tile - 1, Nq - 1) + Nk - Nq)
             if last >= 0:
                 steps = max(steps, last // 128 + 1)
-        out.append((steps + 1, (bh // Hq) * Hkv + (bh % Hq) // (Hq // Hkv)))
+        out.append((steps + 2, (bh // Hq) * Hkv + (bh % Hq) // (Hq // Hkv)))
     return out
 
 
