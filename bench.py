@@ -71,6 +71,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--bwd", action="store_true", help="time the backward pass instead of the forward")
     ap.add_argument("--fp8", action="store_true", help="time the 8-bit (e4m3) forward")
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the timed steps into one CUDA graph and time its replay (launch-bound workloads)")
     return ap.parse_args(argv)
 
 
@@ -482,17 +484,33 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     launches_per_step = 3 if args.bwd else 1
 
-    def step(i):
+    def step(i, s=None):
+        s = stream if s is None else s
         if args.bwd:
             q, k, v, o, lse, do, dq, dk, dv, dl = sets[i % ROTATE]
-            fa.bwd(q, k, v, o, lse, do, causal=prob.causal, scale=prob.scale, stream=stream,
+            fa.bwd(q, k, v, o, lse, do, causal=prob.causal, scale=prob.scale, stream=s,
                    dq=dq, dk=dk, dv=dv, delta=dl)
             return
         q, k, v, o, lse = sets[i % ROTATE]
         if args.fp8:
-            fa.fwd_fp8(q, k, v, *descales, causal=prob.causal, scale=prob.scale, out=o, lse=lse, stream=stream)
+            fa.fwd_fp8(q, k, v, *descales, causal=prob.causal, scale=prob.scale, out=o, lse=lse, stream=s)
             return
-        fa.fwd(q, k, v, causal=prob.causal, scale=prob.scale, cu_seqlens=cu, out=o, lse=lse, stream=stream)
+        fa.fwd(q, k, v, causal=prob.causal, scale=prob.scale, cu_seqlens=cu, out=o, lse=lse, stream=s)
+
+    # --graph: the timed steps are captured into one CUDA graph once (after
+    # the warm-up) and the timed region is its replay, so that host launch
+    # overhead drops out for launch-bound workloads.  The kernels and their
+    # inputs are the same.
+    graph = None
+    if args.graph:
+        for i in range(max(args.warmup, 1)):
+            step(i)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(args.steps):
+                step(i, torch.cuda.current_stream(dev))
+        torch.cuda.synchronize(dev)
 
     fa.fa_device_status()
     sampler = None
@@ -516,8 +534,11 @@ def run_ours(args):
     if sampler:
         sampler.mark_start()
     ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            step(i)
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     if sampler:
@@ -646,7 +667,8 @@ def run_ours(args):
             "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3" if args.fp8 else "bf16", "data": "synthetic",
-            "config": workload_config(prob, name, world, args.bwd, args.fp8),
+            "config": dict(workload_config(prob, name, world, args.bwd, args.fp8),
+                           **({"launch": "one CUDA graph of the timed steps"} if args.graph else {})),
             "roofline": roofline,
             "warm_l2": {"ms_per_step": warm_ms, "value": flops / (warm_ms * 1e-3) / 1e12, "unit": UNIT,
                         "steps": warm_steps, "note": "one input set reused every step; context only"},
