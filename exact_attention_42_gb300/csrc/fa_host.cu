@@ -104,18 +104,30 @@ extern "C" fa_status fa_fwd_host(const void* q_h, const void* k_h, const void* v
 
   const size_t row = static_cast<size_t>(d) * 2;  // bytes of one bf16 row
   const int g = Hq / Hkv;
-  // Pieces: (batch b, key/value heads [h0, h1)); a packed batch is one piece.
+  // Pieces: ranges [u0, u1) of the flattened (batch, key/value head) index
+  // b * Hkv + h, contiguous in every tensor (a range may cross a batch
+  // boundary: the kernel then sees its slices as the heads of one batch).
+  // Sizes fall linearly from the first piece to the last (weights n, n-1,
+  // ..., 1), so that the tail after the last input copy -- the last kernel
+  // and the last output copy -- stays short.  A packed batch is one piece.
   struct Piece {
-    int b, h0, h1;
+    long long u0, u1;
   };
   std::vector<Piece> list;
-  if (packed) {
-    list.push_back(Piece{0, 0, Hkv});
-  } else {
-    const int per_b = (pieces + B - 1) / B;
-    const int step = (Hkv + per_b - 1) / per_b;
-    for (int b = 0; b < B; ++b)
-      for (int h0 = 0; h0 < Hkv; h0 += step) list.push_back(Piece{b, h0, h0 + step < Hkv ? h0 + step : Hkv});
+  const long long units = packed ? 1 : static_cast<long long>(B) * Hkv;
+  {
+    const long long n = units < pieces ? units : pieces;
+    const long long wsum = n * (n + 1) / 2;
+    long long u = 0;
+    for (long long i = 0; i < n; ++i) {
+      // Cumulative share of the first i + 1 weights, rounded; at least one unit per piece.
+      const long long cum = n - 1 - i;  // weights left after this piece: 1 + ... + cum
+      long long end = units - (units * (cum * (cum + 1) / 2) + wsum / 2) / wsum;
+      if (end < u + 1) end = u + 1;
+      if (end > units - (n - 1 - i)) end = units - (n - 1 - i);
+      list.push_back(Piece{u, end});
+      u = end;
+    }
   }
   auto at = [](const void* base, size_t off) {
     return static_cast<void*>(static_cast<char*>(const_cast<void*>(base)) + off);
@@ -124,10 +136,10 @@ extern "C" fa_status fa_fwd_host(const void* q_h, const void* k_h, const void* v
                           cudaMemcpyHostToDevice, cs.in))
     return FA_ERR_CUDA;
   for (const Piece& pc : list) {
-    const int hq = (pc.h1 - pc.h0) * g, hkv = pc.h1 - pc.h0;
+    const int hkv = packed ? Hkv : static_cast<int>(pc.u1 - pc.u0), hq = hkv * g;
     // Dense: the piece's rows are contiguous in every tensor (batch-major, then head).
-    const size_t q_rows0 = packed ? 0 : (static_cast<size_t>(pc.b) * Hq + static_cast<size_t>(pc.h0) * g) * Nq;
-    const size_t kv_rows0 = packed ? 0 : (static_cast<size_t>(pc.b) * Hkv + pc.h0) * static_cast<size_t>(Nk);
+    const size_t q_rows0 = packed ? 0 : static_cast<size_t>(pc.u0) * g * Nq;
+    const size_t kv_rows0 = packed ? 0 : static_cast<size_t>(pc.u0) * static_cast<size_t>(Nk);
     const size_t q_rows = static_cast<size_t>(hq) * Nq, kv_rows = static_cast<size_t>(hkv) * Nk;
     if (!fa::copy(at(q_d, q_rows0 * row), at(q_h, q_rows0 * row), q_rows * row, cudaMemcpyHostToDevice, cs.in) ||
         (Nk > 0 && (!fa::copy(at(k_d, kv_rows0 * row), at(k_h, kv_rows0 * row), kv_rows * row,

@@ -218,9 +218,11 @@ fa_status fa_fp8_quantize(const void* x, void* x8, float* descale, int B, int H,
  * device memory); cu_seqlens_h / cu_seqlens_d: the packed offsets on the host
  * and B+1 int32 of device staging for them (both NULL for a dense problem).
  *
- * A dense problem is cut into about `pieces` (>= 1) slices, each one batch
- * entry with a range of key/value heads and their query heads: contiguous in
- * every tensor.  Each slice's host-to-device copies run on a copy-in stream,
+ * A dense problem is cut into `pieces` (>= 1; at most B * Hkv) slices, each a
+ * range of the flattened (batch, key/value head) index with its query heads:
+ * contiguous in every tensor.  Slice sizes fall linearly from the first to
+ * the last (weights pieces, ..., 2, 1), which keeps the work left after the
+ * last input copy short.  Each slice's host-to-device copies run on a copy-in stream,
  * its fa_fwd launch on `stream` and its device-to-host copies on a copy-out
  * stream (both copy streams belong to the library, one pair per device), so
  * the copies of one slice overlap the kernel and the copies of others.  A
