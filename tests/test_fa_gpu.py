@@ -129,11 +129,15 @@ def test_no_keys(fa, dev):
     assert np.all(o == 0.0) and np.all(np.isneginf(lse))
 
 
-def test_growing_scores_force_rescales(fa, dev):
+@pytest.mark.parametrize("d", [64, 128])
+def test_growing_scores_force_rescales(fa, dev, d):
     """Scores that grow along the key axis move the running max by more than
-    the rescale threshold in every K/V tile (exercises the O correction)."""
-    N, d = 1024, 128
-    # s_j = scale * 0.25 * d * k_j grows by about 20 (log2 units) per 128-key tile.
+    the rescale threshold in every K/V tile (exercises the O correction; at
+    d = 64 the correction first waits for the tile's previous P V product,
+    which runs behind the next QK there)."""
+    N = 1024
+    # s_j = scale * 0.25 * d * k_j grows by about 20 (d = 128) or 14 (d = 64)
+    # log2 units per 128-key tile.
     q = np.full((1, 2, N, d), 0.25)
     ramp = np.linspace(0.0, 40.0, N)[None, None, :, None]
     k = np.broadcast_to(ramp, (1, 2, N, d)) + 0.01 * np.random.default_rng(0).standard_normal((1, 2, N, d))

@@ -179,6 +179,29 @@ def test_fp8_packed_matches_oracle(fa, dev, case):
     _check(o, lse, ref_o, ref_lse, bound, "fp8 packed %s" % (lens,))
 
 
+def test_fp8_d64_growing_scores_force_rescales(fa, dev):
+    """Scores that grow along the key axis move the running max by more than
+    the 8-bit rescale threshold in every K/V tile.  At d = 64 the next QK
+    product runs ahead of the previous P V, so each correction of O first
+    waits for that product."""
+    from fa_inputs import f64_to_bf16_bits
+    N, d = 1024, 64
+    q = np.full((1, 2, N, d), 0.25)
+    ramp = np.linspace(0.0, 40.0, N)[None, None, :, None]
+    k = np.broadcast_to(ramp, (1, 2, N, d)) + 0.01 * np.random.default_rng(0).standard_normal((1, 2, N, d))
+    v = np.random.default_rng(1).standard_normal((1, 2, N, d))
+    for causal in (False, True):
+        p = make_dense(1, 2, 2, N, N, d, seed=0, causal=causal)
+        p.q, p.k, p.v = (f64_to_bf16_bits(x) for x in (q, k, v))
+        p.scale = 1.0 / np.sqrt(d)
+        f8 = make_fp8(p)
+        o, lse = _run(fa, f8, dev)
+        qq, kk, vv = f8.dequantized()
+        ref_o, ref_lse = attention_fwd(qq, kk, vv, p.scale, causal)
+        bound, _ = attention_fwd(qq, kk, np.abs(vv), p.scale, causal)
+        _check(o, lse, ref_o, ref_lse, bound, "fp8 d64 growing scores causal=%s" % causal)
+
+
 def test_fp8_d64_from_bf16_with_rotation(fa, dev):
     """The quantizer and the 8-bit forward at d = 64 together: within the
     8-bit bound of the oracle on the same dequantized, rotated inputs."""
