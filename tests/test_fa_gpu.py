@@ -223,6 +223,47 @@ def test_host_entry_pieces_gqa(fa, dev, chunks):
     assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
 
 
+@pytest.mark.parametrize("chunks", [1, 3])
+@pytest.mark.parametrize("shape", [(2, 16, 4, 1, 3000, 128), (1, 32, 8, 4, 2500, 64)],
+                         ids=["q1-gqa4-d128", "q4-gqa4-d64"])
+def test_host_entry_decode_shapes(fa, dev, shape, chunks):
+    # Few query rows per key/value head (R = group * Nq <= 16): every piece
+    # goes to the split-KV kernel, and every element is checked against the
+    # oracle.  The split count follows the number of (batch, key/value head)
+    # groups in a launch; with at most 8 groups here the whole problem and
+    # every piece take the same splits, so the pieces also match the device
+    # entry bit for bit (with many groups they would not, in the last bits).
+    B, Hq, Hkv, Nq, Nk, d = shape
+    prob = make_dense(B, Hq, Hkv, Nq, Nk, d, seed=16 + Nq, causal=False)
+    qh, kh, vh = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (prob.q, prob.k, prob.v))
+    o_h, l_h = fa.fwd_host(qh, kh, vh, causal=False, chunks=chunks)
+    o_d, l_d = fa.fwd(qh.to(dev), kh.to(dev), vh.to(dev), causal=False)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+    ref_o, ref_lse = oracle_full(prob)
+    compare(o_h.float().numpy().astype(np.float64), l_h.numpy().astype(np.float64), ref_o, ref_lse, "decode host")
+
+
+@pytest.mark.parametrize("chunks", [2, 5])
+def test_host_entry_d64_pieces(fa, dev, chunks):
+    # d = 64, non-causal, Nq != Nk, uneven pieces: the device entry's result
+    # bit for bit, and every element against the oracle.
+    prob = make_dense(3, 10, 5, 333, 190, 64, seed=17, causal=False)
+    qh, kh, vh = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (prob.q, prob.k, prob.v))
+    o_h, l_h = fa.fwd_host(qh, kh, vh, causal=False, chunks=chunks)
+    o_d, l_d = fa.fwd(qh.to(dev), kh.to(dev), vh.to(dev), causal=False)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+    ref_o, ref_lse = oracle_full(prob)
+    compare(o_h.float().numpy().astype(np.float64), l_h.numpy().astype(np.float64), ref_o, ref_lse, "d64 host")
+
+
+def test_host_entry_no_keys(fa, dev):
+    # Nk = 0: no copies of K and V, O = 0 and LSE = -inf for every row.
+    q = torch.randn(2, 4, 70, 128).to(torch.bfloat16).pin_memory()
+    k = torch.empty(2, 2, 0, 128, dtype=torch.bfloat16).pin_memory()
+    o_h, l_h = fa.fwd_host(q, k, k.clone(), causal=False, chunks=3)
+    assert torch.all(o_h == 0) and torch.all(torch.isneginf(l_h))
+
+
 def test_host_entry_packed(fa, dev):
     prob = make_varlen([5, 300, 129, 0, 64], 4, 2, 64, seed=15, causal=True)
     qh, kh, vh = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in (prob.q, prob.k, prob.v))
