@@ -102,6 +102,16 @@ extern "C" fa_status fa_fwd_host(const void* q_h, const void* k_h, const void* v
       cudaStreamWaitEvent(cs.in, start, 0) != cudaSuccess || cudaStreamWaitEvent(cs.out, start, 0) != cudaSuccess)
     return FA_ERR_CUDA;
 
+  // From here on an error still orders later work on `stream` after every
+  // copy already issued on the copy streams (best effort: these calls report
+  // nothing further), so the caller may reuse its buffers once `stream` is done.
+  auto fail = [&](fa_status code) {
+    cudaEvent_t in_end = events.make(), out_end = events.make();
+    if (in_end != nullptr && cudaEventRecord(in_end, cs.in) == cudaSuccess) cudaStreamWaitEvent(stream, in_end, 0);
+    if (out_end != nullptr && cudaEventRecord(out_end, cs.out) == cudaSuccess) cudaStreamWaitEvent(stream, out_end, 0);
+    return code;
+  };
+
   const size_t row = static_cast<size_t>(d) * 2;  // bytes of one bf16 row
   const int g = Hq / Hkv;
   // Pieces: ranges [u0, u1) of the flattened (batch, key/value head) index
@@ -134,7 +144,7 @@ extern "C" fa_status fa_fwd_host(const void* q_h, const void* k_h, const void* v
   };
   if (packed && !fa::copy(cu_seqlens_d, cu_seqlens_h, sizeof(int32_t) * (static_cast<size_t>(B) + 1),
                           cudaMemcpyHostToDevice, cs.in))
-    return FA_ERR_CUDA;
+    return fail(FA_ERR_CUDA);
   for (const Piece& pc : list) {
     const int hkv = packed ? Hkv : static_cast<int>(pc.u1 - pc.u0), hq = hkv * g;
     // Dense: the piece's rows are contiguous in every tensor (batch-major, then head).
@@ -146,29 +156,29 @@ extern "C" fa_status fa_fwd_host(const void* q_h, const void* k_h, const void* v
                               cudaMemcpyHostToDevice, cs.in) ||
                     !fa::copy(at(v_d, kv_rows0 * row), at(v_h, kv_rows0 * row), kv_rows * row,
                               cudaMemcpyHostToDevice, cs.in))))
-      return FA_ERR_CUDA;
+      return fail(FA_ERR_CUDA);
     cudaEvent_t in_done = events.make();
     if (in_done == nullptr || cudaEventRecord(in_done, cs.in) != cudaSuccess ||
         cudaStreamWaitEvent(stream, in_done, 0) != cudaSuccess)
-      return FA_ERR_CUDA;
+      return fail(FA_ERR_CUDA);
     st = fa_fwd(at(q_d, q_rows0 * row), Nk > 0 ? at(k_d, kv_rows0 * row) : nullptr,
                 Nk > 0 ? at(v_d, kv_rows0 * row) : nullptr, at(o_d, q_rows0 * row),
                 static_cast<float*>(at(lse_d, q_rows0 * sizeof(float))), packed ? B : 1, hq, hkv, Nq, Nk, d, scale,
                 causal, packed ? cu_seqlens_d : nullptr, stream);
-    if (st != FA_OK) return st;
+    if (st != FA_OK) return fail(st);
     cudaEvent_t k_done = events.make();
     if (k_done == nullptr || cudaEventRecord(k_done, stream) != cudaSuccess ||
         cudaStreamWaitEvent(cs.out, k_done, 0) != cudaSuccess)
-      return FA_ERR_CUDA;
+      return fail(FA_ERR_CUDA);
     if (!fa::copy(at(o_h, q_rows0 * row), at(o_d, q_rows0 * row), q_rows * row, cudaMemcpyDeviceToHost, cs.out) ||
         !fa::copy(at(lse_h, q_rows0 * sizeof(float)), at(lse_d, q_rows0 * sizeof(float)), q_rows * sizeof(float),
                   cudaMemcpyDeviceToHost, cs.out))
-      return FA_ERR_CUDA;
+      return fail(FA_ERR_CUDA);
   }
   // Later work on `stream` sees O and LSE in host memory.
   cudaEvent_t done = events.make();
   if (done == nullptr || cudaEventRecord(done, cs.out) != cudaSuccess ||
       cudaStreamWaitEvent(stream, done, 0) != cudaSuccess)
-    return FA_ERR_CUDA;
+    return fail(FA_ERR_CUDA);
   return FA_OK;
 }

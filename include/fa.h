@@ -236,8 +236,12 @@ fa_status fa_fp8_quantize(const void* x, void* x8, float* descale, int B, int H,
  * for earlier work on `stream` before it writes the staging buffers.
  * Errors: fa_fwd's argument errors, plus FA_ERR_SHAPE for pieces < 1 and
  * FA_ERR_NULL for a missing host or staging buffer, are reported before
- * anything is enqueued; FA_ERR_CUDA if a copy, stream or event call fails
- * (copies already enqueued then still run).
+ * anything is enqueued; FA_ERR_CUDA if a copy, stream or event call fails.
+ * On an error after the first copy was issued, the copies and kernels
+ * already enqueued still run, and the call still orders later work on
+ * `stream` after them (as far as the CUDA calls for that succeed), so the
+ * buffers may be reused once `stream` is synchronised; O and LSE are then
+ * incomplete.
  */
 fa_status fa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse_h,
                       void* q_d, void* k_d, void* v_d, void* o_d, float* lse_d,
