@@ -146,32 +146,50 @@ def fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
         _, Hkv, Nk, _ = k.shape
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    nb = q.is_pinned()
-    if out is None:
-        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=nb)
-    if lse is None:
-        lse = torch.empty(q.shape[:-1], dtype=torch.float32, pin_memory=nb)
+    if out is None or lse is None:
+        nb = q.is_pinned()  # a driver query: only when outputs are allocated here
+        if out is None:
+            out = torch.empty(q.shape, dtype=q.dtype, pin_memory=nb)
+        if lse is None:
+            lse = torch.empty(q.shape[:-1], dtype=torch.float32, pin_memory=nb)
     if tuple(out.shape) != tuple(q.shape) or out.dtype != torch.bfloat16 or out.is_cuda or not out.is_contiguous():
         raise ValueError("out must be a contiguous bf16 host tensor shaped like q")
     if tuple(lse.shape) != tuple(q.shape[:-1]) or lse.dtype != torch.float32 or lse.is_cuda \
             or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 host tensor of q's leading shape")
-    with torch.cuda.device(device):
-        qd = torch.empty(q.shape, dtype=q.dtype, device=device)
-        kd = torch.empty(k.shape, dtype=k.dtype, device=device)
-        vd = torch.empty(v.shape, dtype=v.dtype, device=device)
-        od = torch.empty(q.shape, dtype=q.dtype, device=device)
-        ld = torch.empty(q.shape[:-1], dtype=torch.float32, device=device)
-        cud = torch.empty(cu_seqlens.shape, dtype=torch.int32, device=device) if packed else None
-        s = torch.cuda.current_stream(device)
-        st = fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                         qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(), ld.data_ptr(),
-                         B, Hq, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
-                         cu_seqlens.data_ptr() if packed else None, cud.data_ptr() if packed else None,
-                         max(1, int(chunks)), s.cuda_stream)
-        if st != 0:
-            raise FaError(st, "fa_fwd_host")
-        s.synchronize()
+    # One staging allocation for Q, K, V, O, LSE (and cu_seqlens), carved at
+    # 256-byte offsets: the C entry needs 16-byte aligned Q, K, V, O and
+    # 4-byte aligned LSE and cu_seqlens.  It lives until the call has waited.
+    sizes = (q.numel() * 2, k.numel() * 2, v.numel() * 2, q.numel() * 2, out.numel() // d * 4,
+             cu_seqlens.numel() * 4 if packed else 0)
+    offs, total = [], 0
+    for n in sizes:
+        offs.append(total)
+        total += (n + 255) // 256 * 256
+    if device.index != torch.cuda.current_device():
+        with torch.cuda.device(device):
+            return _fwd_host_call(q, k, v, out, lse, cu_seqlens, sizes, offs, total, B, Hq, Hkv, Nq, Nk, d, scale,
+                                  causal, chunks, device)
+    return _fwd_host_call(q, k, v, out, lse, cu_seqlens, sizes, offs, total, B, Hq, Hkv, Nq, Nk, d, scale, causal,
+                          chunks, device)
+
+
+def _fwd_host_call(q, k, v, out, lse, cu_seqlens, sizes, offs, total, B, Hq, Hkv, Nq, Nk, d, scale, causal, chunks,
+                   device):
+    """fwd_host's C call on the current device, which is `device`."""
+    stage = torch.empty(max(total, 1), dtype=torch.uint8, device=device)
+    base = stage.data_ptr()
+    qd, kd, vd, od, ld, cud = (base + off if n else 0 for n, off in zip(sizes, offs))
+    packed = cu_seqlens is not None
+    s = torch.cuda.current_stream(device)
+    st = fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                     qd or None, kd or None, vd or None, od or None, ld or None,
+                     B, Hq, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                     cu_seqlens.data_ptr() if packed else None, cud if packed else None,
+                     max(1, int(chunks)), s.cuda_stream)
+    if st != 0:
+        raise FaError(st, "fa_fwd_host")
+    s.synchronize()
     return out, lse
 
 
