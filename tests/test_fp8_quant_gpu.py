@@ -70,6 +70,8 @@ CASES = [
     (1, 1, 8192, 64, True, False, True),
     (1, 2, 4160, 128, False, False, False),
     (1, 1, 8208, 64, False, True, False),
+    (1, 2, 4096, 128, True, False, True),    # rotated d = 128, four launches
+    (2, 1, 2048, 128, True, True, False),    # rotated and transposed
 ]
 
 
