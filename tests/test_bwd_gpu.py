@@ -135,6 +135,26 @@ def test_bwd_workload_sampled(fa, dev, name):
         _check("dv[%d,%d]" % (b, kvh), dv[b, kvh, keys], rv)
 
 
+def test_bwd_workload_full_size(fa, dev):
+    """The bench workload (B2 H32 N4096 d128 causal) at full size: every
+    element of dQ, dK, dV and delta against the oracle, one (batch, head) at a
+    time (one query head per key/value head here, so each slice is a whole
+    problem of its own)."""
+    prob = make_workload("b2_h32_n4096_d128_causal")
+    assert prob.Hq == prob.Hkv
+    do_bits = make_dout(prob, 1000)
+    dq, dk, dv, delta = _run(fa, prob, do_bits, dev)
+    q, k, v, do = (bf16_bits_to_f64(x) for x in (prob.q, prob.k, prob.v, do_bits))
+    for b in range(prob.B):
+        for h in range(prob.Hq):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            rq, rk, rv, rd = attention_bwd(q[sl], k[sl], v[sl], do[sl], prob.scale, prob.causal)
+            _check("dq[%d,%d]" % (b, h), dq[sl], rq)
+            _check("dk[%d,%d]" % (b, h), dk[sl], rk)
+            _check("dv[%d,%d]" % (b, h), dv[sl], rv)
+            _check("delta[%d,%d]" % (b, h), delta[sl], rd)
+
+
 @pytest.mark.parametrize("lens,hq,hkv,d,causal", [
     ([5, 130, 1, 256, 300], 4, 2, 128, True),
     ([0, 129, 128, 64], 2, 2, 64, False),
