@@ -54,7 +54,8 @@ KERNEL_SOURCES = {
                "exact_attention_42_gb300/csrc/fa_sched.cu"],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-ROTATE = 3            # input copies cycled through, so each step reads from HBM
+ROTATE_MIN = 3        # input copies cycled through, so each step reads from HBM
+ROTATE_MAX = 4096
 L2_BYTES = 129 * 2 ** 20
 
 
@@ -325,6 +326,14 @@ def step_bytes(prob, bwd: bool = False, fp8: bool = False) -> int:
     return qkv + out
 
 
+def rotation(prob, bwd: bool = False, fp8: bool = False) -> int:
+    """Input copies the timed steps cycle through: enough that together they
+    hold more than twice the L2, so that each step's inputs come from HBM
+    (at least ROTATE_MIN, at most ROTATE_MAX)."""
+    per = max(1, step_bytes(prob, bwd, fp8))
+    return int(min(ROTATE_MAX, max(ROTATE_MIN, 2 * L2_BYTES // per + 1)))
+
+
 def workload_config(prob, name, world: int = 1, bwd: bool = False, fp8: bool = False):
     cfg = {"workload": name, "B": prob.B, "Hq": prob.Hq, "Hkv": prob.Hkv, "Nq": prob.Nq, "Nk": prob.Nk,
            "d": prob.d, "causal": prob.causal, "flop_per_step": prob.flops()}
@@ -332,8 +341,9 @@ def workload_config(prob, name, world: int = 1, bwd: bool = False, fp8: bool = F
         cfg["seqlens"] = prob.seqlens()
         cfg["total_tokens"] = int(prob.cu_seqlens[-1])
     cfg["parallelism"] = "replicas" if world > 1 else "single"
+    rot = rotation(prob, bwd, fp8)
     cfg["l2"] = "inputs rotated over %d copies (%.0f MB > %d MB L2)" % (
-        ROTATE, ROTATE * step_bytes(prob, bwd, fp8) / 1e6, L2_BYTES // 2 ** 20)
+        rot, rot * step_bytes(prob, bwd, fp8) / 1e6, L2_BYTES // 2 ** 20)
     return cfg
 
 
@@ -468,7 +478,8 @@ def run_ours(args):
     do0 = dev_bf16(make_dout(prob, 1000)) if args.bwd else None
     cu = None if prob.cu_seqlens is None else torch.from_numpy(prob.cu_seqlens).to(dev)
     sets = []
-    for r in range(ROTATE):
+    rotate = rotation(prob, args.bwd, args.fp8)
+    for r in range(rotate):
         q, k, v = (q0, k0, v0) if r == 0 else (q0.clone(), k0.clone(), v0.clone())
         o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=dev)
@@ -487,11 +498,11 @@ def run_ours(args):
     def step(i, s=None):
         s = stream if s is None else s
         if args.bwd:
-            q, k, v, o, lse, do, dq, dk, dv, dl = sets[i % ROTATE]
+            q, k, v, o, lse, do, dq, dk, dv, dl = sets[i % rotate]
             fa.bwd(q, k, v, o, lse, do, causal=prob.causal, scale=prob.scale, stream=s,
                    dq=dq, dk=dk, dv=dv, delta=dl)
             return
-        q, k, v, o, lse = sets[i % ROTATE]
+        q, k, v, o, lse = sets[i % rotate]
         if args.fp8:
             fa.fwd_fp8(q, k, v, *descales, causal=prob.causal, scale=prob.scale, out=o, lse=lse, stream=s)
             return

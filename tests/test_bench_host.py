@@ -83,6 +83,24 @@ def test_workload_config_and_flops():
     assert cfg["flop_per_step"] == 4 * 2 * (9 + 25) * 64
 
 
+def test_rotated_inputs_exceed_l2():
+    # The timed steps cycle through enough input copies that together they
+    # hold more than twice the L2 (shape-only stand-ins of the dense workloads;
+    # step_bytes reads only the array sizes and the head dim).
+    from types import SimpleNamespace
+    from fa_inputs import WORKLOADS
+    for name, w in WORKLOADS.items():
+        if w["kind"] != "dense":
+            continue
+        arr = lambda h, n: SimpleNamespace(size=w["B"] * h * n * w["d"])
+        prob = SimpleNamespace(q=arr(w["Hq"], w["Nq"]), k=arr(w["Hkv"], w["Nk"]), v=arr(w["Hkv"], w["Nk"]), d=w["d"])
+        for bwd in (False, True):
+            for fp8 in (False, True):
+                rot = bench.rotation(prob, bwd, fp8)
+                assert bench.ROTATE_MIN <= rot <= bench.ROTATE_MAX, name
+                assert rot == bench.ROTATE_MAX or rot * bench.step_bytes(prob, bwd, fp8) > 2 * bench.L2_BYTES, name
+
+
 def test_oracle_sample_reports_threads():
     from fa_inputs import make_dense
     prob = make_dense(1, 2, 2, 64, 64, 64, seed=1, causal=True)
