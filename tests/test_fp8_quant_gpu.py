@@ -72,6 +72,9 @@ CASES = [
     (1, 1, 8208, 64, False, True, False),
     (1, 2, 4096, 128, True, False, True),    # rotated d = 128, four launches
     (2, 1, 2048, 128, True, True, False),    # rotated and transposed
+    # Tensors near or above the L2 size (the GQA N16384 inputs).
+    (1, 32, 16384, 128, False, True, False),  # 134 MB, transposed
+    (1, 26, 16384, 128, True, False, False),  # 109 MB, rotated
 ]
 
 
